@@ -1,0 +1,184 @@
+"""ctypes wrappers around the C oracle (``fs_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY -- see the package docstring.  Every function takes
+and returns numpy arrays.  bf16 tensors are passed as their raw uint16 words.
+
+Citations are to "FlashSampling: Fast and Memory-Efficient Exact Sampling"
+(arXiv 2603.15854): the Gumbel-max rule and its single-pass online form (method
+section, Algorithm I.1 in the Appendix), the exactness statement (a tiled
+argmax returns the same maximizer as a full Gumbel-max pass, Appendix C), and
+the LM-head GEMM of the IO-model section.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+NO_NOISE = 1
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        u64, i64, u32, i32 = ctypes.c_uint64, ctypes.c_int64, ctypes.c_uint32, ctypes.c_int
+        vp = ctypes.c_void_p
+        lib.oracle_philox4x64_10.argtypes = [vp, vp, vp]
+        lib.oracle_philox4x64_10.restype = None
+        lib.oracle_noise_word.argtypes = [u64, u64, i64, i64]
+        lib.oracle_noise_word.restype = u32
+        lib.oracle_uniform.argtypes = [u32]
+        lib.oracle_uniform.restype = ctypes.c_double
+        lib.oracle_gumbel_from_word.argtypes = [u32]
+        lib.oracle_gumbel_from_word.restype = ctypes.c_float
+        lib.oracle_gumbel.argtypes = [u64, u64, i64, i64]
+        lib.oracle_gumbel.restype = ctypes.c_float
+        lib.oracle_noise_block.argtypes = [u64, u64, i64, i64, i64, i64, vp, vp, i32]
+        lib.oracle_noise_block.restype = None
+        lib.oracle_uniform_block.argtypes = [vp, i64, vp]
+        lib.oracle_uniform_block.restype = None
+        lib.oracle_gumbel_block.argtypes = [vp, i64, vp, i32]
+        lib.oracle_gumbel_block.restype = None
+        lib.oracle_logits.argtypes = [vp, vp, i64, i64, i64, vp, i32]
+        lib.oracle_logits.restype = None
+        lib.oracle_sample_from_logits.argtypes = [vp, i64, i64, vp, u64, u64, u32,
+                                                  vp, vp, vp, vp, i32]
+        lib.oracle_sample_from_logits.restype = None
+        lib.oracle_sample.argtypes = [vp, vp, i64, i64, i64, vp, u64, u64, u32,
+                                      vp, vp, vp, vp, i32]
+        lib.oracle_sample.restype = None
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses by default."""
+    return int(_load().oracle_num_threads())
+
+
+def philox4x64_10(counter, key):
+    """One Philox4x64-10 block (SC'11): counter [4] uint64, key [2] uint64."""
+    c = _c(counter, np.uint64)
+    k = _c(key, np.uint64)
+    out = np.zeros(4, dtype=np.uint64)
+    _load().oracle_philox4x64_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def noise_word(seed, offset, b, v) -> int:
+    return int(_load().oracle_noise_word(seed, offset, b, v))
+
+
+def uniform(x) -> float:
+    return float(_load().oracle_uniform(x))
+
+
+def gumbel_from_word(x) -> float:
+    return float(_load().oracle_gumbel_from_word(x))
+
+
+def gumbel(seed, offset, b, v) -> float:
+    return float(_load().oracle_gumbel(seed, offset, b, v))
+
+
+def uniform_block(words):
+    """u for each 32-bit word (float64, exact)."""
+    x = _c(words, np.uint32)
+    u = np.zeros(x.shape, dtype=np.float64)
+    _load().oracle_uniform_block(_ptr(x), x.size, _ptr(u))
+    return u
+
+
+def gumbel_block(words, nthreads=0):
+    """g for each 32-bit word (f32)."""
+    x = _c(words, np.uint32)
+    g = np.zeros(x.shape, dtype=np.float32)
+    _load().oracle_gumbel_block(_ptr(x), x.size, _ptr(g), nthreads)
+    return g
+
+
+def noise_block(seed, offset, b0, nb, v0, nv, nthreads=0):
+    """Random words and Gumbels for rows [b0, b0+nb) x vocab [v0, v0+nv)."""
+    words = np.zeros((nb, nv), dtype=np.uint32)
+    g = np.zeros((nb, nv), dtype=np.float32)
+    _load().oracle_noise_block(seed, offset, b0, nb, v0, nv, _ptr(words), _ptr(g),
+                               nthreads)
+    return words, g
+
+
+def logits(H_bits, W_bits, nthreads=0):
+    """fp64 logits H W^T from raw bf16 words H [B, D] and W [V, D]."""
+    H = _c(H_bits, np.uint16)
+    W = _c(W_bits, np.uint16)
+    B, D = H.shape
+    V, D2 = W.shape
+    assert D == D2
+    out = np.zeros((B, V), dtype=np.float64)
+    _load().oracle_logits(_ptr(H), _ptr(W), B, V, D, _ptr(out), nthreads)
+    return out
+
+
+def _temps(T, B):
+    T = np.asarray(T, dtype=np.float32)
+    if T.ndim == 0:
+        T = np.full(B, T, dtype=np.float32)
+    assert T.shape == (B,)
+    return np.ascontiguousarray(T)
+
+
+def sample_from_logits(l32, T, seed, offset, flags=0, want_scores=False, nthreads=0):
+    """Full Gumbel-max pass over given f32 logits [B, V].
+
+    Returns (idx int64 [B], best f32 [B], second f32 [B], scores or None).
+    """
+    L = _c(l32, np.float32)
+    B, V = L.shape
+    Tv = _temps(T, B)
+    idx = np.zeros(B, dtype=np.int64)
+    best = np.zeros(B, dtype=np.float32)
+    second = np.zeros(B, dtype=np.float32)
+    scores = np.zeros((B, V), dtype=np.float32) if want_scores else None
+    _load().oracle_sample_from_logits(_ptr(L), B, V, _ptr(Tv), seed, offset, flags,
+                                      _ptr(idx), _ptr(best), _ptr(second),
+                                      _ptr(scores), nthreads)
+    return idx, best, second, scores
+
+
+def sample(H_bits, W_bits, T, seed, offset, flags=0, want_logits=False, nthreads=0):
+    """The whole path from bf16 H [B, D] and W [V, D].
+
+    Returns (idx int64 [B], best f32 [B], second f32 [B], logits64 or None).
+    """
+    H = _c(H_bits, np.uint16)
+    W = _c(W_bits, np.uint16)
+    B, D = H.shape
+    V, D2 = W.shape
+    assert D == D2
+    Tv = _temps(T, B)
+    idx = np.zeros(B, dtype=np.int64)
+    best = np.zeros(B, dtype=np.float32)
+    second = np.zeros(B, dtype=np.float32)
+    l64 = np.zeros((B, V), dtype=np.float64) if want_logits else None
+    _load().oracle_sample(_ptr(H), _ptr(W), B, V, D, _ptr(Tv), seed, offset, flags,
+                          _ptr(idx), _ptr(best), _ptr(second), _ptr(l64), nthreads)
+    return idx, best, second, l64
+
+
+__all__ = ["NO_NOISE", "num_threads", "philox4x64_10", "noise_word", "uniform",
+           "gumbel_from_word", "gumbel", "uniform_block", "gumbel_block", "noise_block", "logits",
+           "sample_from_logits", "sample"]

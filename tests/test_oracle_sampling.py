@@ -1,0 +1,228 @@
+"""Pins for the oracle's logits and its Gumbel-max pass.
+
+FlashSampling (arXiv 2603.15854) fixes the result as the maximizer of the
+perturbed logits s_i = l~_i + g_i over the whole vocabulary (method section;
+exactness by Appendix C: argmax decomposes over a partition), which is an exact
+sample from softmax(l~) with l~ = l / T.  The checks below pin the oracle to
+things outside itself: a numpy fp64 matmul, exact integer arithmetic, brute
+force on tiny vocabularies, partition invariance, the softmax law by
+chi-squared tests and quadrature, and the temperature's placement.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.integrate
+import scipy.special
+import scipy.stats
+import torch
+
+import oracle
+import workloads
+
+
+def bf16_bits(x):
+    return workloads.to_bits(torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16))
+
+
+def bits_to_f64(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- logits
+
+@pytest.mark.parametrize("B,V,D", [(3, 50, 1), (2, 33, 7), (5, 129, 64), (4, 300, 257)])
+def test_logits_match_numpy_fp64_matmul(B, V, D):
+    rng = np.random.default_rng(B * 1000 + D)
+    H = bf16_bits(rng.standard_normal((B, D)))
+    W = bf16_bits(0.05 * rng.standard_normal((V, D)))
+    got = oracle.logits(H, W)
+    Hf, Wf = bits_to_f64(H), bits_to_f64(W)
+    want = Hf @ Wf.T
+    scale = np.abs(Hf) @ np.abs(Wf).T
+    assert np.all(np.abs(got - want) <= 4 * D * 2.0 ** -53 * scale + 1e-300)
+
+
+def test_logits_exact_on_small_integers():
+    """Small integers are exact in bf16; the sums are exact integers."""
+    rng = np.random.default_rng(3)
+    B, V, D = 3, 17, 45
+    Hi = rng.integers(-8, 9, size=(B, D))
+    Wi = rng.integers(-8, 9, size=(V, D))
+    got = oracle.logits(bf16_bits(Hi), bf16_bits(Wi))
+    for b in range(B):
+        for v in range(V):
+            want = sum(int(Hi[b, k]) * int(Wi[v, k]) for k in range(D))
+            assert got[b, v] == want
+
+
+def test_sample_uses_f32_rounded_logits():
+    """oracle.sample == oracle.sample_from_logits on f32(logits)."""
+    rng = np.random.default_rng(11)
+    B, V, D = 6, 200, 96
+    H = bf16_bits(rng.standard_normal((B, D)))
+    W = bf16_bits(0.1 * rng.standard_normal((V, D)))
+    T = np.array([1.0, 0.5, 1.5, 0.7, 2.0, 1.0], dtype=np.float32)
+    i1, s1, t1, l64 = oracle.sample(H, W, T, 42, 9, want_logits=True)
+    i2, s2, t2, _ = oracle.sample_from_logits(l64.astype(np.float32), T, 42, 9)
+    assert np.array_equal(i1, i2)
+    assert np.array_equal(s1, s2) and np.array_equal(t1, t2)
+    assert np.array_equal(l64, oracle.logits(H, W))
+
+
+# ---------------------------------------------------------------- argmax
+
+def brute_force_row(l32, T, seed, offset, b):
+    """Independent restatement on tiny V: enumerate (v, s_v) and pick the max."""
+    invT = np.float32(1.0) / np.float32(T)
+    pairs = []
+    for v in range(len(l32)):
+        g = np.float32(oracle.gumbel(seed, offset, b, v))
+        s = np.float32(np.float32(l32[v]) * invT) + g
+        pairs.append((float(np.float32(s)), v))
+    best = max(pairs, key=lambda p: (p[0], -p[1]))
+    rest = [p[0] for p in pairs if p[1] != best[1]]
+    return best[1], best[0], max(rest) if rest else -math.inf
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 5, 8])
+def test_brute_force_tiny_vocab(V):
+    rng = np.random.default_rng(V)
+    B = 64
+    L = rng.standard_normal((B, V)).astype(np.float32)
+    T = rng.uniform(0.5, 1.5, size=B).astype(np.float32)
+    idx, best, second, _ = oracle.sample_from_logits(L, T, 1234, 77)
+    for b in range(B):
+        i, s, s2 = brute_force_row(L[b], T[b], 1234, 77, b)
+        assert idx[b] == i and best[b] == np.float32(s)
+        assert second[b] == np.float32(s2)
+
+
+def test_partition_invariance():
+    """argmax over the whole row == max over the per-block maxima, for random
+    contiguous and scattered partitions (ties resolved to the lowest index)."""
+    rng = np.random.default_rng(5)
+    B, V = 16, 1000
+    L = rng.standard_normal((B, V)).astype(np.float32)
+    L[:, 500] = L[:, 100]  # exact logit ties
+    idx, best, _, S = oracle.sample_from_logits(L, 1.0, 9, 0, want_scores=True)
+    for trial in range(50):
+        if trial % 2 == 0:
+            cuts = np.sort(rng.choice(np.arange(1, V), size=rng.integers(1, 40), replace=False))
+            blocks = np.split(np.arange(V), cuts)
+        else:
+            perm = rng.permutation(V)
+            blocks = np.array_split(perm, rng.integers(2, 30))
+        for b in range(B):
+            cands = []
+            for blk in blocks:
+                blk = np.sort(blk)
+                j = blk[np.argmax(S[b, blk])]  # np.argmax: first occurrence
+                cands.append((S[b, j], -j))
+            s, negj = max(cands)
+            assert -negj == idx[b] and s == best[b]
+
+
+def test_ties_go_to_lowest_index_without_noise():
+    L = np.zeros((4, 64), dtype=np.float32)
+    L[0, [5, 9, 40]] = 3.0
+    L[1, :] = 1.0
+    L[2, [63, 62]] = 2.0
+    L[3, [0, 63]] = -1.0
+    L[3, 1:63] = -2.0
+    idx, best, second, _ = oracle.sample_from_logits(L, 1.0, 0, 0, flags=oracle.NO_NOISE)
+    assert list(idx) == [5, 0, 62, 0]
+    assert list(best) == [3.0, 1.0, 2.0, -1.0]
+    assert list(second) == [3.0, 1.0, 2.0, -1.0]  # equal runner-up => gap 0
+
+
+def test_invalid_temperature_and_nonfinite_logits():
+    L = np.ones((6, 16), dtype=np.float32)
+    T = np.array([0.0, -1.0, np.inf, np.nan, 1.0, 1.0], dtype=np.float32)
+    L[4, :] = np.nan
+    L[5, :] = -np.inf
+    L[5, 7] = 0.0
+    idx, best, second, _ = oracle.sample_from_logits(L, T, 3, 0)
+    assert list(idx[:4]) == [-1, -1, -1, -1]
+    assert np.all(np.isnan(best[:4])) and np.all(np.isnan(second[:4]))
+    assert idx[4] == -1 and best[4] == -np.inf  # NaN never wins
+    assert idx[5] == 7  # the only finite score wins
+
+
+def test_temperature_divides_logits_before_the_noise():
+    """T = 2 is exact in f32: sample(l, T=2) == sample(l/2, T=1) bit for bit,
+    and differs from argmax(l + g) (noise added before the division)."""
+    rng = np.random.default_rng(8)
+    L = (3 * rng.standard_normal((4096, 16))).astype(np.float32)
+    a = oracle.sample_from_logits(L, 2.0, 21, 4)[0]
+    b = oracle.sample_from_logits(L / np.float32(2.0), 1.0, 21, 4)[0]
+    c = oracle.sample_from_logits(L, 1.0, 21, 4)[0]
+    assert np.array_equal(a, b)
+    assert np.count_nonzero(a != c) > 100
+
+
+# ---------------------------------------------------------------- distribution
+
+def chisq_pvalue(counts, probs):
+    n = counts.sum()
+    exp = probs * n
+    # merge categories with expected count < 5 into one bucket
+    small = exp < 5
+    if small.any():
+        counts = np.append(counts[~small], counts[small].sum())
+        exp = np.append(exp[~small], exp[small].sum())
+        if exp[-1] == 0:
+            counts, exp = counts[:-1], exp[:-1]
+    return scipy.stats.chisquare(counts, exp).pvalue
+
+
+def softmax_f32_transform(l, T):
+    invT = np.float32(1.0) / np.float32(T)
+    lt = (l.astype(np.float32) * invT).astype(np.float64)
+    return scipy.special.softmax(lt)
+
+
+@pytest.mark.parametrize("V", [2, 8, 64])
+@pytest.mark.parametrize("T", [0.5, 1.0, 1.5])
+def test_frequencies_match_softmax_across_rows(V, T):
+    """10^5 draws (one per row, distinct Philox counters) vs softmax(l/T)."""
+    rng = np.random.default_rng(100 * V + int(10 * T))
+    l = (1.5 * rng.standard_normal(V)).astype(np.float32)
+    N = 100_000
+    L = np.broadcast_to(l, (N, V))
+    idx = oracle.sample_from_logits(L, T, 0xC0FFEE + V, 0)[0]
+    counts = np.bincount(idx, minlength=V).astype(np.float64)
+    assert chisq_pvalue(counts, softmax_f32_transform(l, T)) > 0.01
+
+
+def test_frequencies_match_softmax_across_offsets():
+    """10^5 decode steps (offset = step) of one row vs softmax(l/T)."""
+    V, T, N = 8, 0.8, 100_000
+    l = np.array([0.3, -1.0, 2.0, 0.0, 1.1, -0.4, 0.9, 2.0], dtype=np.float32)
+    counts = np.zeros(V)
+    for off in range(N):
+        counts[oracle.sample_from_logits(l[None, :], T, 0xABCD, off)[0][0]] += 1
+    assert chisq_pvalue(counts, softmax_f32_transform(l, T)) > 0.01
+
+
+def test_duplicates_sampled_with_equal_frequency():
+    V, N = 16, 100_000
+    l = np.linspace(-1, 1, V).astype(np.float32)
+    l[9] = l[3]
+    l[15] = l[3]
+    idx = oracle.sample_from_logits(np.broadcast_to(l, (N, V)), 1.0, 0xD00D, 0)[0]
+    c = np.bincount(idx, minlength=V)
+    trio = np.array([c[3], c[9], c[15]], dtype=np.float64)
+    assert scipy.stats.chisquare(trio).pvalue > 0.01
+
+
+def test_gumbel_max_law_by_quadrature():
+    """P(i wins) = int pdf(x - l_i) prod_{j != i} F(x - l_j) dx equals
+    softmax(l)_i: the law the chi-squared tests compare against."""
+    l = np.array([0.5, -1.0, 2.0, 0.1])
+    pdf = lambda x: np.exp(-x - np.exp(-x))
+    cdf = lambda x: np.exp(-np.exp(-x))
+    for i in range(len(l)):
+        f = lambda x: pdf(x - l[i]) * np.prod([cdf(x - l[j]) for j in range(len(l)) if j != i])
+        p, _ = scipy.integrate.quad(f, -20, 40, limit=200)
+        assert abs(p - scipy.special.softmax(l)[i]) < 1e-8
