@@ -1,0 +1,495 @@
+// fs_api.cu -- host side of the C ABI declared in include/fs_sample.h:
+// argument validation, the Stage 1 schedule, TMA tensor-map encoding, the
+// cached workspace of fs_sample, and the launches.  All compute runs in the
+// kernels of fs_stage1.cu and fs_small.cu; nothing here computes on the host.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "../../include/fs_sample.h"
+#include "fs_internal.h"
+
+namespace fs {
+
+// ------------------------------------------------------------------ errors
+static thread_local std::string t_last_error = "no error";
+
+static fs_status fail(fs_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+static fs_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(FS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------------ schedule
+// Stage 1 schedule.  nM batch tiles of 128 rows; the vocabulary is cut into P
+// contiguous partitions, balanced in 16-row units, with P * nM <= SM count so
+// that each CTA streams a 1/P share of W once.  CTA c takes batch tile c % nM
+// and partition c / nM: the nM CTAs that share a partition run side by side
+// and read the same W tiles, so W comes from HBM about once.
+bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *p) {
+    if (B < 1 || V < 1 || D < 1 || num_sms < 1) return false;
+    p->B = B;
+    p->V = V;
+    p->D = D;
+    const int64_t nM = (B + kBM - 1) / kBM;
+    const int64_t U = (V + kUnitRows - 1) / kUnitRows;
+    int64_t P = num_sms / nM;
+    if (P < 1) P = 1;
+    if (P > U) P = U;
+    p->nM = static_cast<int>(nM);
+    p->U = U;
+    p->P = static_cast<int>(P);
+    p->G = static_cast<int>(P * nM);
+    p->nCand = static_cast<int>(2 * P);
+    const int64_t max_units = (U + P - 1) / P;
+    p->maxTiles = static_cast<int>((max_units * kUnitRows + kBN - 1) / kBN);
+    p->nChunks = static_cast<int>((V + kLogitsChunk - 1) / kLogitsChunk);
+    const int64_t slots = p->nCand > p->nChunks ? p->nCand : p->nChunks;
+    const int64_t region = ((slots * B * 4) + 255) / 256 * 256;
+    p->wsBytes = static_cast<size_t>(2 * region);
+    return true;
+}
+
+// Candidate buffers inside a workspace: scores, then indices.
+static void split_workspace(const Plan &p, void *ws, float **score, int32_t **idx) {
+    const int64_t slots = p.nCand > p.nChunks ? p.nCand : p.nChunks;
+    const int64_t region = ((slots * p.B * 4) + 255) / 256 * 256;
+    *score = static_cast<float *>(ws);
+    *idx = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + region);
+}
+
+// ------------------------------------------------------------------ device info
+struct DeviceInfo {
+    bool known = false;
+    int sms = 0;
+    int major = 0, minor = 0;
+};
+static std::mutex g_dev_mu;
+static DeviceInfo g_dev[64];
+
+static fs_status device_info(int *dev_out, DeviceInfo *info) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(FS_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.known) {
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(major)");
+        if ((e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(minor)");
+        d.known = true;
+    }
+    if (d.major != 10 || d.minor != 3)
+        return fail(FS_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                    dev, d.major, d.minor);
+    *dev_out = dev;
+    *info = d;
+    return FS_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] read in boxes of 64 columns x box_rows
+// rows, 128-byte swizzled in shared memory; out-of-range elements read as 0.
+static fs_status make_tmap(CUtensorMap *map, const void *base, int64_t rows, int64_t cols,
+                           uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(FS_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FS_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld x %lld] box %u",
+                    static_cast<int>(r), static_cast<long long>(rows),
+                    static_cast<long long>(cols), box_rows);
+    return FS_OK;
+}
+
+// ------------------------------------------------------------------ validation
+static bool temperature_ok(float T) { return isfinite(T) && T > 0.0f; }
+
+static fs_status validate_shape(int64_t B, int64_t V, int64_t D) {
+    if (B < 1 || V < 1 || D < 1)
+        return fail(FS_ERR_INVALID_ARG, "B, V and D must be >= 1 (got %lld, %lld, %lld)",
+                    static_cast<long long>(B), static_cast<long long>(V),
+                    static_cast<long long>(D));
+    if (V > FS_MAX_VOCAB) return fail(FS_ERR_UNSUPPORTED, "V=%lld exceeds 2^31-1", static_cast<long long>(V));
+    if (B > FS_MAX_BATCH) return fail(FS_ERR_UNSUPPORTED, "B=%lld exceeds 2^24", static_cast<long long>(B));
+    if (D % 8 != 0)
+        return fail(FS_ERR_UNSUPPORTED, "D=%lld must be a multiple of 8 (16-byte rows)",
+                    static_cast<long long>(D));
+    if (D > (1 << 20)) return fail(FS_ERR_UNSUPPORTED, "D=%lld exceeds 2^20", static_cast<long long>(D));
+    return FS_OK;
+}
+
+static fs_status validate_gemm_inputs(const void *H, const void *W, int64_t B, int64_t V,
+                                      int64_t D) {
+    if (!H || !W) return fail(FS_ERR_INVALID_ARG, "H and W must be non-null device pointers");
+    fs_status st = validate_shape(B, V, D);
+    if (st != FS_OK) return st;
+    if (reinterpret_cast<uintptr_t>(H) % 16 || reinterpret_cast<uintptr_t>(W) % 16)
+        return fail(FS_ERR_UNSUPPORTED, "H and W must be 16-byte aligned");
+    return FS_OK;
+}
+
+static fs_status validate_temperature(float temperature, const float *temperatures) {
+    if (!temperatures && !temperature_ok(temperature))
+        return fail(FS_ERR_INVALID_ARG,
+                    "temperature must be finite and > 0 (got %g); greedy decoding is not "
+                    "supported",
+                    static_cast<double>(temperature));
+    return FS_OK;
+}
+
+static fs_status validate_workspace(const Plan &p, const void *ws, size_t bytes) {
+    if (!ws) return fail(FS_ERR_INVALID_ARG, "workspace must be non-null");
+    if (reinterpret_cast<uintptr_t>(ws) % 16)
+        return fail(FS_ERR_UNSUPPORTED, "workspace must be 16-byte aligned");
+    if (bytes < p.wsBytes)
+        return fail(FS_ERR_NO_MEMORY, "workspace of %zu bytes is smaller than the %zu needed",
+                    bytes, p.wsBytes);
+    return FS_OK;
+}
+
+static uint64_t wait_timeout_ns() {
+    static uint64_t ns = [] {
+        const char *s = getenv("FS_WAIT_TIMEOUT_MS");
+        const long long ms = s ? atoll(s) : 0;
+        return ms > 0 ? static_cast<uint64_t>(ms) * 1000000ull : 4000000000ull;
+    }();
+    return ns;
+}
+
+// ------------------------------------------------------------------ Stage 1 launch
+static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &p,
+                            float temperature, const float *temperatures, uint64_t seed,
+                            uint64_t offset, uint32_t flags, float *out_logits, void *out_y,
+                            int y_dtype, float *cand_score, int32_t *cand_idx,
+                            cudaStream_t stream) {
+    CUtensorMap tmH, tmW64, tmW16;
+    fs_status st;
+    if ((st = make_tmap(&tmH, H, p.B, p.D, kBM)) != FS_OK) return st;
+    if ((st = make_tmap(&tmW64, W, p.V, p.D, 64)) != FS_OK) return st;
+    if ((st = make_tmap(&tmW16, W, p.V, p.D, 16)) != FS_OK) return st;
+    Stage1Args a;
+    a.B = static_cast<int32_t>(p.B);
+    a.V = static_cast<int32_t>(p.V);
+    a.D = static_cast<int32_t>(p.D);
+    a.nM = p.nM;
+    a.P = p.P;
+    a.U = p.U;
+    a.temps = temperatures;
+    a.temp_scalar = temperature;
+    a.seed = seed;
+    a.offset = offset;
+    a.flags = flags;
+    a.cand_score = cand_score;
+    a.cand_idx = cand_idx;
+    a.out_logits = out_logits;
+    a.out_y = out_y;
+    const void *dst = out_logits ? static_cast<const void *>(out_logits) : out_y;
+    const bool f32 = (mode == kModeSampleStore) || (mode == kModeGemmF32 && y_dtype == FS_DTYPE_F32);
+    a.y_vec_ok = dst && (reinterpret_cast<uintptr_t>(dst) % 16 == 0) &&
+                 (f32 ? (p.V % 4 == 0) : (p.V % 8 == 0));
+    a.timeout_ns = wait_timeout_ns();
+    cudaError_t e = launch_stage1(mode, tmH, tmW64, tmW16, a, p.G, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "Stage 1 launch");
+    return FS_OK;
+}
+
+// ------------------------------------------------------------------ workspace cache
+struct CachedWs {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+static std::mutex g_ws_mu;
+static std::map<std::pair<int, void *>, CachedWs> g_ws;
+
+static fs_status cached_workspace(int dev, cudaStream_t stream, size_t need, void **out) {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    CachedWs &c = g_ws[std::make_pair(dev, static_cast<void *>(stream))];
+    if (c.bytes < need) {
+        size_t grow = 65536;
+        while (grow < need) grow <<= 1;
+        if (c.ptr) {
+            cudaError_t e = cudaFreeAsync(c.ptr, stream);
+            c.ptr = nullptr;
+            c.bytes = 0;
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(workspace)");
+        }
+        cudaError_t e = cudaMallocAsync(&c.ptr, grow, stream);
+        if (e != cudaSuccess) {
+            c.ptr = nullptr;
+            return fail(FS_ERR_NO_MEMORY, "cudaMallocAsync(%zu) failed: %s", grow,
+                        cudaGetErrorString(e));
+        }
+        c.bytes = grow;
+    }
+    *out = c.ptr;
+    return FS_OK;
+}
+
+}  // namespace fs
+
+using namespace fs;
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char *fs_version(void) { return "fs_sample 0.1.0 (sm_103a: TMA + tcgen05 + TMEM)"; }
+
+const char *fs_last_error_string(void) { return t_last_error.c_str(); }
+
+fs_status fs_plan_info(int64_t B, int64_t V, int64_t D, int num_sms, int64_t out[6]) {
+    if (!out) return fail(FS_ERR_INVALID_ARG, "out must be non-null");
+    fs_status st = validate_shape(B, V, D);
+    if (st != FS_OK) return st;
+    if (num_sms < 1) return fail(FS_ERR_INVALID_ARG, "num_sms must be >= 1");
+    Plan p;
+    make_plan(B, V, D, num_sms, &p);
+    out[0] = p.nM;
+    out[1] = p.P;
+    out[2] = p.G;
+    out[3] = p.nCand;
+    out[4] = static_cast<int64_t>(p.wsBytes);
+    out[5] = p.maxTiles;
+    return FS_OK;
+}
+
+size_t fs_workspace_size(int64_t B, int64_t V, int64_t D) {
+    if (validate_shape(B, V, D) != FS_OK) return 0;
+    int dev;
+    DeviceInfo info;
+    if (device_info(&dev, &info) != FS_OK) return 0;
+    Plan p;
+    make_plan(B, V, D, info.sms, &p);
+    return p.wsBytes;
+}
+
+fs_status fs_stage1(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                    float temperature, const float *temperatures, uint64_t seed,
+                    uint64_t offset, uint32_t flags, float *out_logits, void *workspace,
+                    size_t ws_bytes, void *stream) {
+    fs_status st;
+    if ((st = validate_gemm_inputs(H, W, B, V, D)) != FS_OK) return st;
+    if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
+    if (flags & ~(FS_FLAG_NO_NOISE | FS_FLAG_STORE_LOGITS))
+        return fail(FS_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+    if ((flags & FS_FLAG_STORE_LOGITS) && !out_logits)
+        return fail(FS_ERR_INVALID_ARG, "FS_FLAG_STORE_LOGITS needs out_logits");
+    int dev;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    Plan p;
+    make_plan(B, V, D, info.sms, &p);
+    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    float *cs;
+    int32_t *ci;
+    split_workspace(p, workspace, &cs, &ci);
+    const int mode = (flags & FS_FLAG_STORE_LOGITS) ? kModeSampleStore : kModeSample;
+    return run_stage1(mode, H, W, p, temperature, temperatures, seed, offset, flags,
+                      (flags & FS_FLAG_STORE_LOGITS) ? out_logits : nullptr, nullptr, 0, cs, ci,
+                      static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_stage2(int64_t B, int64_t V, int64_t D, float temperature,
+                    const float *temperatures, int64_t *out_idx, float *out_score,
+                    const void *workspace, size_t ws_bytes, void *stream) {
+    fs_status st;
+    if ((st = validate_shape(B, V, D)) != FS_OK) return st;
+    if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
+    if (!out_idx) return fail(FS_ERR_INVALID_ARG, "out_idx must be non-null");
+    int dev;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    Plan p;
+    make_plan(B, V, D, info.sms, &p);
+    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    float *cs;
+    int32_t *ci;
+    split_workspace(p, const_cast<void *>(workspace), &cs, &ci);
+    cudaError_t e = launch_stage2(cs, ci, p.nCand, B, temperatures, temperature, out_idx,
+                                  out_score, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "Stage 2 launch");
+    return FS_OK;
+}
+
+fs_status fs_sample_ex(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                       float temperature, const float *temperatures, uint64_t seed,
+                       uint64_t offset, uint32_t flags, int64_t *out_idx, float *out_score,
+                       float *out_logits, void *workspace, size_t ws_bytes, void *stream) {
+    if (!out_idx) return fail(FS_ERR_INVALID_ARG, "out_idx must be non-null");
+    fs_status st = fs_stage1(H, W, B, V, D, temperature, temperatures, seed, offset, flags,
+                             out_logits, workspace, ws_bytes, stream);
+    if (st != FS_OK) return st;
+    return fs_stage2(B, V, D, temperature, temperatures, out_idx, out_score, workspace, ws_bytes,
+                     stream);
+}
+
+fs_status fs_sample(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                    float temperature, const float *temperatures, uint64_t seed,
+                    uint64_t offset, int64_t *out_idx, float *out_score, void *stream) {
+    fs_status st;
+    if ((st = validate_gemm_inputs(H, W, B, V, D)) != FS_OK) return st;
+    if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
+    if (!out_idx) return fail(FS_ERR_INVALID_ARG, "out_idx must be non-null");
+    int dev;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    Plan p;
+    make_plan(B, V, D, info.sms, &p);
+    void *ws = nullptr;
+    if ((st = cached_workspace(dev, static_cast<cudaStream_t>(stream), p.wsBytes, &ws)) != FS_OK)
+        return st;
+    return fs_sample_ex(H, W, B, V, D, temperature, temperatures, seed, offset, 0, out_idx,
+                        out_score, nullptr, ws, p.wsBytes, stream);
+}
+
+fs_status fs_logits_gemm(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                         void *Y, int y_dtype, void *stream) {
+    fs_status st;
+    if ((st = validate_gemm_inputs(H, W, B, V, D)) != FS_OK) return st;
+    if (!Y) return fail(FS_ERR_INVALID_ARG, "Y must be non-null");
+    if (y_dtype != FS_DTYPE_BF16 && y_dtype != FS_DTYPE_F32)
+        return fail(FS_ERR_INVALID_ARG, "y_dtype must be FS_DTYPE_BF16 or FS_DTYPE_F32");
+    int dev;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    Plan p;
+    make_plan(B, V, D, info.sms, &p);
+    return run_stage1(y_dtype == FS_DTYPE_F32 ? kModeGemmF32 : kModeGemmBf16, H, W, p, 1.0f,
+                      nullptr, 0, 0, 0, nullptr, Y, y_dtype, nullptr, nullptr,
+                      static_cast<cudaStream_t>(stream));
+}
+
+fs_status fs_sample_from_logits(const void *Y, int y_dtype, int64_t B, int64_t V,
+                                float temperature, const float *temperatures, uint64_t seed,
+                                uint64_t offset, uint32_t flags, int64_t *out_idx,
+                                float *out_score, void *workspace, size_t ws_bytes,
+                                void *stream) {
+    fs_status st;
+    if (!Y) return fail(FS_ERR_INVALID_ARG, "Y must be non-null");
+    if (y_dtype != FS_DTYPE_BF16 && y_dtype != FS_DTYPE_F32)
+        return fail(FS_ERR_INVALID_ARG, "y_dtype must be FS_DTYPE_BF16 or FS_DTYPE_F32");
+    if ((st = validate_shape(B, V, 8)) != FS_OK) return st;
+    if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
+    if (flags & ~FS_FLAG_NO_NOISE)
+        return fail(FS_ERR_INVALID_ARG, "only FS_FLAG_NO_NOISE applies to materialised logits");
+    if (!out_idx) return fail(FS_ERR_INVALID_ARG, "out_idx must be non-null");
+    int dev;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    Plan p;
+    make_plan(B, V, 8, info.sms, &p);
+    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    float *cs;
+    int32_t *ci;
+    split_workspace(p, workspace, &cs, &ci);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_logits_sample(Y, y_dtype, B, V, temperatures, temperature, seed,
+                                         offset, flags, cs, ci, p.nChunks, s);
+    if (e != cudaSuccess) return cuda_fail(e, "logits sampling launch");
+    e = launch_stage2(cs, ci, p.nChunks, B, temperatures, temperature, out_idx, out_score, s);
+    if (e != cudaSuccess) return cuda_fail(e, "Stage 2 launch");
+    return FS_OK;
+}
+
+fs_status fs_sample_unfused(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                            float temperature, const float *temperatures, uint64_t seed,
+                            uint64_t offset, void *Y, int y_dtype, int64_t *out_idx,
+                            float *out_score, void *workspace, size_t ws_bytes, void *stream) {
+    fs_status st;
+    if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
+    if (!out_idx) return fail(FS_ERR_INVALID_ARG, "out_idx must be non-null");
+    if ((st = fs_logits_gemm(H, W, B, V, D, Y, y_dtype, stream)) != FS_OK) return st;
+    return fs_sample_from_logits(Y, y_dtype, B, V, temperature, temperatures, seed, offset, 0,
+                                 out_idx, out_score, workspace, ws_bytes, stream);
+}
+
+fs_status fs_debug_noise(uint64_t seed, uint64_t offset, int64_t b0, int64_t nb, int64_t V,
+                         uint32_t *out_words, float *out_g, void *stream) {
+    if (b0 < 0 || nb < 1 || V < 1)
+        return fail(FS_ERR_INVALID_ARG, "need b0 >= 0, nb >= 1, V >= 1");
+    if (!out_words && !out_g) return fail(FS_ERR_INVALID_ARG, "no output requested");
+    int dev;
+    DeviceInfo info;
+    fs_status st = device_info(&dev, &info);
+    if (st != FS_OK) return st;
+    cudaError_t e = launch_debug_noise(seed, offset, b0, nb, V, out_words, out_g,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "debug noise launch");
+    return FS_OK;
+}
+
+fs_status fs_get_device_status(void *stream, uint32_t *out_word) {
+    int dev;
+    DeviceInfo info;
+    fs_status st = device_info(&dev, &info);
+    if (st != FS_OK) return st;
+    uint32_t w = 0;
+    cudaError_t e = read_and_clear_status(static_cast<cudaStream_t>(stream), &w);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    if (out_word) *out_word = w;
+    if (w) return fail(FS_ERR_TIMEOUT, "a bounded wait inside Stage 1 expired (word 0x%x)", w);
+    return FS_OK;
+}
+
+fs_status fs_release_workspaces(void) {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    fs_status st = FS_OK;
+    for (auto &kv : g_ws) {
+        if (!kv.second.ptr) continue;
+        cudaSetDevice(kv.first.first);
+        cudaError_t e = cudaFree(kv.second.ptr);
+        if (e != cudaSuccess && st == FS_OK) st = cuda_fail(e, "cudaFree(workspace)");
+    }
+    g_ws.clear();
+    cudaSetDevice(cur);
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// fs_internal.h -- declarations shared by the library's translation units.
+// Not part of the public C ABI (include/fs_sample.h is).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fs {
+
+// ---- Stage 1 tiling ------------------------------------------------------
+// One CTA per SM, persistent over its share of the vocabulary.  A tile is
+// 128 batch rows (MMA M, TMEM lanes) x up to 256 vocabulary rows (MMA N, TMEM
+// columns); K advances 64 bf16 (one 128-byte swizzle span) per pipeline stage.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kUmmaK = 16;
+constexpr int kABytes = kBM * kBK * 2;  // 16 KiB: H tile
+constexpr int kBBytes = kBN * kBK * 2;  // 32 KiB: W tile
+constexpr int kNumEpiWarps = 8;         // 2 per TMEM lane quarter
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;  // two 256-column accumulators
+constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 1024 + 256;
+constexpr int kUnitRows = 16;  // vocabulary partitions are multiples of 16 rows
+
+// ---- materialised-logits sampler ------------------------------------------
+constexpr int kLogitsChunk = 8192;  // vocabulary entries per block
+constexpr int kLogitsThreads = 256;
+
+enum Stage1Mode : int {
+    kModeSample = 0,       // fused: GEMM + temperature + Gumbel + tile argmax
+    kModeSampleStore = 1,  // same, plus f32 logits written to HBM
+    kModeGemmBf16 = 2,     // unfused GEMM: Y written as bf16, no sampling
+    kModeGemmF32 = 3,      // unfused GEMM: Y written as f32, no sampling
+};
+
+struct Plan {
+    int64_t B, V, D;
+    int nM;        // batch tiles of 128 rows
+    int P;         // vocabulary partitions (one per CTA column)
+    int G;         // CTAs launched = P * nM
+    int nCand;     // candidate slots per row (2 per partition: two column halves)
+    int64_t U;     // vocabulary units of 16 rows
+    int maxTiles;  // max vocabulary tiles per CTA
+    int nChunks;   // blocks per row of the materialised-logits sampler
+    size_t wsBytes;
+};
+
+bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *plan);
+
+struct Stage1Args {
+    int32_t B, V, D;
+    int32_t nM, P;
+    int64_t U;
+    const float *temps;  // nullable device [B]
+    float temp_scalar;
+    uint64_t seed, offset;
+    uint32_t flags;
+    float *cand_score;  // [nCand][B]
+    int32_t *cand_idx;  // [nCand][B]
+    float *out_logits;  // [B][V] f32 (kModeSampleStore)
+    void *out_y;        // [B][V] bf16/f32 (GEMM modes)
+    int y_vec_ok;       // row starts of Y / out_logits are 16-byte aligned
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const CUtensorMap &tmW64,
+                          const CUtensorMap &tmW16, const Stage1Args &a, int grid,
+                          cudaStream_t stream);
+
+cudaError_t launch_stage2(const float *cand_score, const int32_t *cand_idx, int nCand,
+                          int64_t B, const float *temps, float temp_scalar, int64_t *out_idx,
+                          float *out_score, cudaStream_t stream);
+
+cudaError_t launch_logits_sample(const void *Y, int y_dtype, int64_t B, int64_t V,
+                                 const float *temps, float temp_scalar, uint64_t seed,
+                                 uint64_t offset, uint32_t flags, float *cand_score,
+                                 int32_t *cand_idx, int nChunks, cudaStream_t stream);
+
+cudaError_t launch_debug_noise(uint64_t seed, uint64_t offset, int64_t b0, int64_t nb,
+                               int64_t V, uint32_t *out_words, float *out_g,
+                               cudaStream_t stream);
+
+// Device error word of Stage 1 (bit 0: a bounded wait expired).
+cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *word);
+
+}  // namespace fs

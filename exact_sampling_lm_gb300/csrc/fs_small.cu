@@ -1,0 +1,231 @@
+// fs_small.cu -- the small kernels around Stage 1:
+//   * Stage 2 ("FlashSampling: Fast and Memory-Efficient Exact Sampling",
+//     method section, "Stage 2 (Reduction)"): argmax over the candidate
+//     buffer of shape [candidate slots, B], one warp per row;
+//   * the sampling pass of the unfused comparator (the IO-model section's
+//     baseline: "sample from the logits" after a GEMM materialised them);
+//   * a debug kernel exposing the epilogue's noise for tests.
+// All of them use the same noise functions and tie rule as Stage 1: higher
+// score wins, equal scores go to the lower vocabulary index, NaN never wins.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fs_internal.h"
+#include "fs_noise.cuh"
+
+namespace fs {
+
+namespace {
+
+// (s, i) beats (best, bi)?  Indices compare as unsigned so that the "no
+// candidate" index -1 loses every tie.
+__device__ __forceinline__ bool better(float s, uint32_t i, float best, uint32_t bi) {
+    return s > best || (s == best && i < bi);
+}
+
+__device__ __forceinline__ void warp_argmax(float &best, uint32_t &bi) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        const float s = __shfl_xor_sync(0xffffffffu, best, d);
+        const uint32_t i = __shfl_xor_sync(0xffffffffu, bi, d);
+        if (better(s, i, best, bi)) {
+            best = s;
+            bi = i;
+        }
+    }
+}
+
+__device__ __forceinline__ bool temperature_ok(float T) { return isfinite(T) && T > 0.0f; }
+
+}  // namespace
+
+// ------------------------------------------------------------------ Stage 2
+constexpr int kStage2Warps = 8;
+
+__global__ void __launch_bounds__(kStage2Warps * 32)
+    stage2_kernel(const float *__restrict__ cand_score, const int32_t *__restrict__ cand_idx,
+                  int nCand, int64_t B, const float *__restrict__ temps, float temp_scalar,
+                  int64_t *__restrict__ out_idx, float *__restrict__ out_score) {
+    const int lane = threadIdx.x & 31;
+    const int64_t b = static_cast<int64_t>(blockIdx.x) * kStage2Warps + (threadIdx.x >> 5);
+    if (b >= B) return;
+    float best = -INFINITY;
+    uint32_t bi = 0xFFFFFFFFu;
+    for (int i = lane; i < nCand; i += 32) {
+        const float s = cand_score[static_cast<int64_t>(i) * B + b];
+        const uint32_t id = static_cast<uint32_t>(cand_idx[static_cast<int64_t>(i) * B + b]);
+        if (better(s, id, best, bi)) {
+            best = s;
+            bi = id;
+        }
+    }
+    warp_argmax(best, bi);
+    if (lane == 0) {
+        const float T = temps ? temps[b] : temp_scalar;
+        const bool ok = temperature_ok(T);
+        out_idx[b] = (ok && bi != 0xFFFFFFFFu) ? static_cast<int64_t>(bi) : -1;
+        if (out_score) out_score[b] = ok ? best : __int_as_float(0x7fc00000);
+    }
+}
+
+cudaError_t launch_stage2(const float *cand_score, const int32_t *cand_idx, int nCand,
+                          int64_t B, const float *temps, float temp_scalar, int64_t *out_idx,
+                          float *out_score, cudaStream_t stream) {
+    const int64_t blocks = (B + kStage2Warps - 1) / kStage2Warps;
+    stage2_kernel<<<static_cast<unsigned>(blocks), kStage2Warps * 32, 0, stream>>>(
+        cand_score, cand_idx, nCand, B, temps, temp_scalar, out_idx, out_score);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ unfused sampling pass
+// Block (chunk, row): 256 threads scan kLogitsChunk logits of one row, 8 per
+// thread per step (one Philox call), then reduce to one candidate.
+template <typename T>
+__device__ __forceinline__ void load8(const T *row, int64_t v, int64_t v_end, bool vec_ok,
+                                      float (&l)[8]);
+
+template <>
+__device__ __forceinline__ void load8<float>(const float *row, int64_t v, int64_t v_end,
+                                             bool vec_ok, float (&l)[8]) {
+    if (vec_ok && v + 8 <= v_end) {
+        const float4 a = __ldcs(reinterpret_cast<const float4 *>(row + v));
+        const float4 b = __ldcs(reinterpret_cast<const float4 *>(row + v + 4));
+        l[0] = a.x; l[1] = a.y; l[2] = a.z; l[3] = a.w;
+        l[4] = b.x; l[5] = b.y; l[6] = b.z; l[7] = b.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) l[e] = (v + e < v_end) ? row[v + e] : 0.0f;
+    }
+}
+
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *row, int64_t v,
+                                                     int64_t v_end, bool vec_ok, float (&l)[8]) {
+    if (vec_ok && v + 8 <= v_end) {
+        const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(row + v));
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            l[2 * j] = __uint_as_float(w[j] << 16);
+            l[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            l[e] = (v + e < v_end) ? __bfloat162float(row[v + e]) : 0.0f;
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kLogitsThreads)
+    logits_sample_kernel(const T *__restrict__ Y, int64_t B, int64_t V,
+                         const float *__restrict__ temps, float temp_scalar, uint64_t seed,
+                         uint64_t offset, uint32_t flags, float *__restrict__ cand_score,
+                         int32_t *__restrict__ cand_idx, int nChunks, bool vec_ok) {
+    __shared__ float red_s[kLogitsThreads / 32];
+    __shared__ uint32_t red_i[kLogitsThreads / 32];
+    const int chunk = blockIdx.x;
+    const bool no_noise = (flags & 1u) != 0;
+    for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
+        const float Tb = temps ? temps[b] : temp_scalar;
+        const bool t_ok = temperature_ok(Tb);
+        const float invT = __frcp_rn(Tb);
+        const int64_t v_begin = static_cast<int64_t>(chunk) * kLogitsChunk;
+        const int64_t v_end = min(V, v_begin + kLogitsChunk);
+        const T *row = Y + b * V;
+        float best = -INFINITY;
+        uint32_t bi = 0xFFFFFFFFu;
+        if (t_ok) {
+            for (int64_t v = v_begin + threadIdx.x * 8; v < v_end; v += kLogitsThreads * 8) {
+                float l[8];
+                load8<T>(row, v, v_end, vec_ok, l);
+                uint32_t x[8];
+                if (!no_noise) noise_words8(seed, offset, static_cast<uint64_t>(b),
+                                            static_cast<uint64_t>(v) >> 3, x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float g = no_noise ? 0.0f : gumbel_from_word(x[e]);
+                    const float s = __fadd_rn(__fmul_rn(l[e], invT), g);
+                    if (v + e < v_end && s > best) {
+                        best = s;
+                        bi = static_cast<uint32_t>(v + e);
+                    }
+                }
+            }
+        }
+        warp_argmax(best, bi);
+        const int w = threadIdx.x >> 5;
+        if ((threadIdx.x & 31) == 0) {
+            red_s[w] = best;
+            red_i[w] = bi;
+        }
+        __syncthreads();
+        if (w == 0) {
+            best = (threadIdx.x < kLogitsThreads / 32) ? red_s[threadIdx.x] : -INFINITY;
+            bi = (threadIdx.x < kLogitsThreads / 32) ? red_i[threadIdx.x] : 0xFFFFFFFFu;
+            warp_argmax(best, bi);
+            if (threadIdx.x == 0) {
+                cand_score[static_cast<int64_t>(chunk) * B + b] = best;
+                cand_idx[static_cast<int64_t>(chunk) * B + b] = static_cast<int32_t>(bi);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_logits_sample(const void *Y, int y_dtype, int64_t B, int64_t V,
+                                 const float *temps, float temp_scalar, uint64_t seed,
+                                 uint64_t offset, uint32_t flags, float *cand_score,
+                                 int32_t *cand_idx, int nChunks, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(nChunks), static_cast<unsigned>(B < 65535 ? B : 65535));
+    const uintptr_t base = reinterpret_cast<uintptr_t>(Y);
+    if (y_dtype == 1) {
+        const bool vec_ok = (base % 16 == 0) && (V % 4 == 0);
+        logits_sample_kernel<float><<<grid, kLogitsThreads, 0, stream>>>(
+            static_cast<const float *>(Y), B, V, temps, temp_scalar, seed, offset, flags,
+            cand_score, cand_idx, nChunks, vec_ok);
+    } else {
+        const bool vec_ok = (base % 16 == 0) && (V % 8 == 0);
+        logits_sample_kernel<__nv_bfloat16><<<grid, kLogitsThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(Y), B, V, temps, temp_scalar, seed, offset, flags,
+            cand_score, cand_idx, nChunks, vec_ok);
+    }
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ debug noise
+__global__ void debug_noise_kernel(uint64_t seed, uint64_t offset, int64_t b0, int64_t nb,
+                                   int64_t V, uint32_t *__restrict__ out_words,
+                                   float *__restrict__ out_g) {
+    const int64_t groups = (V + 7) / 8;
+    const int64_t total = nb * groups;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t rb = i / groups;
+        const int64_t v8 = i % groups;
+        uint32_t x[8];
+        noise_words8(seed, offset, static_cast<uint64_t>(b0 + rb), static_cast<uint64_t>(v8), x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int64_t v = v8 * 8 + e;
+            if (v < V) {
+                if (out_words) out_words[rb * V + v] = x[e];
+                if (out_g) out_g[rb * V + v] = gumbel_from_word(x[e]);
+            }
+        }
+    }
+}
+
+cudaError_t launch_debug_noise(uint64_t seed, uint64_t offset, int64_t b0, int64_t nb,
+                               int64_t V, uint32_t *out_words, float *out_g,
+                               cudaStream_t stream) {
+    const int64_t total = nb * ((V + 7) / 8);
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    if (blocks < 1) blocks = 1;
+    debug_noise_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(seed, offset, b0, nb, V,
+                                                                          out_words, out_g);
+    return cudaGetLastError();
+}
+
+}  // namespace fs

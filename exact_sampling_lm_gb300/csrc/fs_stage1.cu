@@ -1,0 +1,386 @@
+// fs_stage1.cu -- Stage 1 of FlashSampling on sm_103a: the LM-head GEMM
+// fused with temperature, Gumbel noise and a per-row tile argmax.
+//
+// "FlashSampling: Fast and Memory-Efficient Exact Sampling", method section:
+// Stage 1 computes one batch tile and one vocabulary tile on chip, applies the
+// deterministic transforms, adds Gumbel noise and keeps the tile-local
+// maximizer for each row; each threadblock handles a contiguous vocabulary
+// chunk.  Only (score, index) candidates leave the chip, never the [B, V]
+// logits.
+//
+// GB300 design (one persistent CTA per SM, 320 threads):
+//   warp 8      TMA producer: streams H [128 x 64] and W [<=256 x 64] k-blocks
+//               (128-byte swizzled) into a 4-stage shared-memory ring.
+//   warp 9      allocates 512 TMEM columns; one thread issues
+//               tcgen05.mma (M=128, N<=256, K=16, bf16 -> f32) into one of two
+//               256-column accumulators and commits to mbarriers.
+//   warps 0-7   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lane quarter w % 4, column half w / 4), then per element
+//               s = l * (1/T) + g with g from Philox4x64-10, and a running
+//               per-row argmax across all tiles of the CTA.  The epilogue of
+//               tile t overlaps the MMA of tile t+1 (double-buffered TMEM).
+// Batch rows sit on the MMA M dimension, so each epilogue thread owns one row
+// and scans the vocabulary in increasing order: the lowest-index tie rule and
+// the 8-wide Philox block both fall out without cross-thread exchange.
+// CTA c works on batch tile c % nM and vocabulary partition c / nM
+// (partitions are balanced in 16-row units), and writes one candidate per
+// (row, partition, column half).
+//
+// Every wait is bounded: on expiry the CTA raises the device error word,
+// tells its other warps to stop, drains its own TMA loads and MMAs, frees TMEM
+// and returns.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fs_internal.h"
+#include "fs_noise.cuh"
+#include "fs_ptx.cuh"
+
+namespace fs {
+
+__device__ uint32_t g_status_word = 0;
+
+namespace {
+
+constexpr uint32_t kStatusTimeout = 1u;
+
+__device__ __forceinline__ int round_up16(int x) { return (x + 15) & ~15; }
+
+__device__ __forceinline__ void raise_timeout(volatile int *abort_flag) {
+    atomicOr(&g_status_word, kStatusTimeout);
+    *abort_flag = 1;
+}
+
+// Stores n (<= 32) consecutive f32 values of one row.
+__device__ __forceinline__ void store_f32_chunk(float *dst, int n, const uint32_t (&r)[32],
+                                                bool vec_ok) {
+    if (vec_ok && n == 32) {
+        float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < n) dst[i] = __uint_as_float(r[i]);
+    }
+}
+
+// Stores n (<= 32) consecutive values of one row rounded to bf16.
+__device__ __forceinline__ void store_bf16_chunk(__nv_bfloat16 *dst, int n,
+                                                 const uint32_t (&r)[32], bool vec_ok) {
+    if (vec_ok && n == 32) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t p[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                __nv_bfloat162 two = __floats2bfloat162_rn(__uint_as_float(r[8 * i + 2 * j]),
+                                                           __uint_as_float(r[8 * i + 2 * j + 1]));
+                p[j] = *reinterpret_cast<uint32_t *>(&two);
+            }
+            d4[i] = make_uint4(p[0], p[1], p[2], p[3]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < n) dst[i] = __float2bfloat16_rn(__uint_as_float(r[i]));
+    }
+}
+
+}  // namespace
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    stage1_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW64,
+                  const __grid_constant__ CUtensorMap tmW16, const Stage1Args a) {
+    constexpr bool kSample = (MODE == kModeSample || MODE == kModeSampleStore);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + kStages * kABytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + kStages * kBBytes);
+    uint64_t *full_bar = bars;
+    uint64_t *empty_bar = bars + kStages;
+    uint64_t *tfull_bar = bars + 2 * kStages;
+    uint64_t *tempty_bar = tfull_bar + 2;
+    uint64_t *done_bar = tempty_bar + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done_bar + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int m = blockIdx.x % a.nM;
+    const int part = blockIdx.x / a.nM;
+    const int64_t u0 = static_cast<int64_t>(part) * a.U / a.P;
+    const int64_t u1 = static_cast<int64_t>(part + 1) * a.U / a.P;
+    const int r0 = static_cast<int>(u0 * kUnitRows);
+    const int r1 = static_cast<int>(min(u1 * kUnitRows, static_cast<int64_t>(a.V)));
+    const int ntiles = (r1 > r0) ? (r1 - r0 + kBN - 1) / kBN : 0;
+    const int nk = (a.D + kBK - 1) / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull_bar[i], 1);
+            mbar_init(&tempty_bar[i], kNumEpiWarps);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == kWarpTma) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tmH);
+            prefetch_tmap(&tmW64);
+            prefetch_tmap(&tmW16);
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_h = l2_policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0;      // stages that received at least one load
+            uint32_t last_phase_bits = 0;  // phase of the last load per stage
+            bool ok = true;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int v0 = r0 + t * kBN;
+                const int tn16 = round_up16(min(kBN, r1 - v0));
+                const int n64 = tn16 >> 6;
+                const int n16 = (tn16 & 63) >> 4;
+                const uint32_t bytes = kABytes + tn16 * (kBK * 2);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, a.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full_bar[stage], bytes);
+                    uint8_t *dA = sA + stage * kABytes;
+                    uint8_t *dB = sB + stage * kBBytes;
+                    const int kx = kb * kBK;
+                    tma_load_2d(dA, &tmH, &full_bar[stage], kx, m * kBM, pol_h);
+                    for (int j = 0; j < n64; ++j)
+                        tma_load_2d(dB + j * 64 * (kBK * 2), &tmW64, &full_bar[stage], kx,
+                                    v0 + j * 64, pol_w);
+                    for (int j = 0; j < n16; ++j)
+                        tma_load_2d(dB + (n64 * 64 + j * 16) * (kBK * 2), &tmW16, &full_bar[stage],
+                                    kx, v0 + n64 * 64 + j * 16, pol_w);
+                    issued_mask |= 1u << stage;
+                    last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) raise_timeout(abort_flag);
+            // Drain: every issued load must land before the CTA's shared
+            // memory is released (immediate on the normal path).
+            for (int s = 0; s < kStages; ++s)
+                if (issued_mask & (1u << s))
+                    mbar_wait_bounded(&full_bar[s], (last_phase_bits >> s) & 1u, a.timeout_ns,
+                                      nullptr);
+        }
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int acc = t & 1;
+                const uint32_t aphase = static_cast<uint32_t>(t >> 1) & 1u;
+                if (!mbar_wait_bounded(&tempty_bar[acc], aphase ^ 1u, a.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const int v0 = r0 + t * kBN;
+                const int tn16 = round_up16(min(kBN, r1 - v0));
+                const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(tn16));
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait_bounded(&full_bar[stage], phase, a.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_addr = smem_u32(sA + stage * kABytes);
+                    const uint32_t b_addr = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+                    for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
+                        umma_bf16_ss(d_tmem, sw128_kmajor_desc(a_addr + ks * kUmmaK * 2),
+                                     sw128_kmajor_desc(b_addr + ks * kUmmaK * 2), idesc,
+                                     (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(&empty_bar[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) umma_commit(&tfull_bar[acc]);
+            }
+            if (!ok) raise_timeout(abort_flag);
+            // Retire every MMA this thread issued before TMEM is freed.
+            umma_commit(done_bar);
+            mbar_wait_bounded(done_bar, 0, a.timeout_ns, nullptr);
+        }
+    } else {
+        // ------------------------------------------------ epilogue warps
+        const int q = warp & 3;  // TMEM lane quarter
+        const int h = warp >> 2; // column half of the tile
+        const int row = q * 32 + lane;
+        const int b = m * kBM + row;
+        const bool warp_has_rows = (m * kBM + q * 32) < a.B;
+        const bool row_ok = b < a.B;
+        float invT = 0.0f;
+        bool t_ok = false;
+        if (kSample && row_ok) {
+            const float T = a.temps ? a.temps[b] : a.temp_scalar;
+            t_ok = isfinite(T) && T > 0.0f;
+            invT = __frcp_rn(T);
+        }
+        const bool no_noise = (a.flags & 1u) != 0;
+        float best = -INFINITY;
+        int bidx = -1;
+        bool ok = true;
+        for (int t = 0; t < ntiles; ++t) {
+            const int acc = t & 1;
+            const uint32_t aphase = static_cast<uint32_t>(t >> 1) & 1u;
+            if (!mbar_wait_bounded(&tfull_bar[acc], aphase, a.timeout_ns, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const int v0 = r0 + t * kBN;
+            const int tn = min(kBN, r1 - v0);
+            const int c_lo = h * (kBN / 2);
+            const int c_hi = min(c_lo + kBN / 2, tn);
+            if (warp_has_rows) {
+                for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32_wait(tmem_base + static_cast<uint32_t>(acc * kBN + c0) +
+                                       (static_cast<uint32_t>(q * 32) << 16),
+                                   r);
+                    const int n_valid = min(32, tn - c0);
+                    const int vbase = v0 + c0;
+                    if (kSample) {
+                        if (row_ok && t_ok) {
+#pragma unroll
+                            for (int g8 = 0; g8 < 4; ++g8) {
+                                if (g8 * 8 < n_valid) {
+                                    uint32_t x[8];
+                                    if (!no_noise)
+                                        noise_words8(a.seed, a.offset, static_cast<uint64_t>(b),
+                                                     static_cast<uint64_t>(vbase + g8 * 8) >> 3, x);
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        const int i = g8 * 8 + e;
+                                        const float l = __uint_as_float(r[i]);
+                                        const float g = no_noise ? 0.0f : gumbel_from_word(x[e]);
+                                        const float s = __fadd_rn(__fmul_rn(l, invT), g);
+                                        if (i < n_valid && s > best) {
+                                            best = s;
+                                            bidx = vbase + i;
+                                        }
+                                    }
+                                }
+                            }
+                        }
+                        if (MODE == kModeSampleStore && row_ok)
+                            store_f32_chunk(a.out_logits + static_cast<size_t>(b) * a.V + vbase,
+                                            n_valid, r, a.y_vec_ok != 0);
+                    } else if (row_ok) {
+                        if (MODE == kModeGemmF32)
+                            store_f32_chunk(static_cast<float *>(a.out_y) +
+                                                static_cast<size_t>(b) * a.V + vbase,
+                                            n_valid, r, a.y_vec_ok != 0);
+                        else
+                            store_bf16_chunk(static_cast<__nv_bfloat16 *>(a.out_y) +
+                                                 static_cast<size_t>(b) * a.V + vbase,
+                                             n_valid, r, a.y_vec_ok != 0);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+        }
+        if (!ok) raise_timeout(abort_flag);
+        if (kSample && row_ok) {
+            const size_t slot = static_cast<size_t>(part) * 2 + h;
+            a.cand_score[slot * a.B + b] = best;
+            a.cand_idx[slot * a.B + b] = bidx;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == kWarpMma) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <int MODE>
+static cudaError_t launch_mode(const CUtensorMap &tmH, const CUtensorMap &tmW64,
+                               const CUtensorMap &tmW16, const Stage1Args &a, int grid,
+                               cudaStream_t stream) {
+    static int configured_mask = 0;  // per device (device ordinals < 32)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 32 && !(configured_mask & (1 << dev))) {
+        e = cudaFuncSetAttribute(stage1_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured_mask |= 1 << dev;
+    }
+    stage1_kernel<MODE><<<grid, kThreads, kSmemBytes, stream>>>(tmH, tmW64, tmW16, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const CUtensorMap &tmW64,
+                          const CUtensorMap &tmW16, const Stage1Args &a, int grid,
+                          cudaStream_t stream) {
+    switch (mode) {
+        case kModeSample: return launch_mode<kModeSample>(tmH, tmW64, tmW16, a, grid, stream);
+        case kModeSampleStore:
+            return launch_mode<kModeSampleStore>(tmH, tmW64, tmW16, a, grid, stream);
+        case kModeGemmBf16: return launch_mode<kModeGemmBf16>(tmH, tmW64, tmW16, a, grid, stream);
+        case kModeGemmF32: return launch_mode<kModeGemmF32>(tmH, tmW64, tmW16, a, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *word) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    uint32_t w = 0;
+    e = cudaMemcpyFromSymbol(&w, g_status_word, sizeof(w));
+    if (e != cudaSuccess) return e;
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+    *word = w;
+    return cudaSuccess;
+}
+
+}  // namespace fs

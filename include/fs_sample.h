@@ -1,0 +1,203 @@
+/*
+ * fs_sample.h -- C ABI of the GB300 (sm_103a) fused LM-head + exact sampling
+ * library (libfs_sample.so).
+ *
+ * The operation ("FlashSampling: Fast and Memory-Efficient Exact Sampling",
+ * arXiv 2603.15854):
+ *   - the LM-head GEMM l = H W^T with H [B, D] hidden states and W [V, D]
+ *     vocabulary-major weights, both bf16 (experimental setup: "Inputs and
+ *     weights are in BF16");
+ *   - exact categorical sampling from softmax(l / T) by the Gumbel-max trick:
+ *     draw i.i.d. Gumbels g, form s = l/T + g, return argmax s (method
+ *     section, Algorithm I.1 of the Appendix);
+ *   - fused in two stages (method section, "Stage 1 (Fused Kernel)" /
+ *     "Stage 2 (Reduction)"): Stage 1 computes logits tile by tile on chip,
+ *     applies the temperature, adds the noise and keeps one maximizer per row
+ *     and per vocabulary tile, never writing the [B, V] logits to HBM; Stage 2
+ *     reduces the small candidate buffer to one token per row.  Exactness:
+ *     argmax decomposes over a partition of the vocabulary (Appendix C).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named H, W, Y, out_*, temperatures and workspace are DEVICE
+ *     pointers into memory the caller owns.  The library never frees them and
+ *     keeps none of them after the call returns.
+ *   - H and W must be 16-byte aligned and D must be a multiple of 8 (the
+ *     tensor-memory-access unit needs 16-byte rows); otherwise the call
+ *     returns FS_ERR_UNSUPPORTED and launches nothing.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on `stream`: a returned FS_OK means the
+ *     work was enqueued; device-side errors surface at the caller's next
+ *     synchronisation or through fs_get_device_status().
+ *   - A bad argument returns an error status and launches nothing.  The reason
+ *     is available from fs_last_error_string() (thread-local).
+ *   - The sampled token of row b is a deterministic function of
+ *     (H[b], W, T_b, seed, offset, b).  A decoder advances `offset` per step.
+ *   - Noise: element (b, v) draws 32 random bits from Philox4x64-10 (Salmon et
+ *     al., SC'11) with key (seed, 0) and counter (v >> 3, b, offset, 0): half
+ *     (v & 1) of 64-bit output word (v & 7) >> 1.  u = ((x >> 8) | 1) * 2^-24,
+ *     g = -log(-log(u)).  The score is s = fl(fl(l * fl(1/T)) + g) in f32.
+ *     Ties in s go to the lowest vocabulary index; NaN never wins.
+ *   - Temperatures: `temperature` (scalar) is used when `temperatures` is
+ *     NULL, otherwise `temperatures` is a device f32 [B] array of per-row
+ *     values.  A scalar that is not finite or not > 0 is rejected with
+ *     FS_ERR_INVALID_ARG.  A per-row value that is not finite or not > 0 gives
+ *     that row out_idx = -1 and out_score = NaN (greedy decoding is not part
+ *     of the method).
+ */
+#ifndef FS_SAMPLE_H
+#define FS_SAMPLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fs_status {
+    FS_OK = 0,
+    FS_ERR_INVALID_ARG = 1, /* null pointer, size < 1, bad scalar temperature  */
+    FS_ERR_UNSUPPORTED = 2, /* alignment / D % 8 / size limits / no device      */
+    FS_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed              */
+    FS_ERR_TIMEOUT = 4,     /* a kernel gave up a bounded wait (device word)     */
+    FS_ERR_NO_MEMORY = 5,   /* workspace allocation failed or is too small       */
+} fs_status;
+
+/* Flags of fs_sample_ex / fs_stage1 / fs_sample_from_logits. */
+#define FS_FLAG_NO_NOISE 0x1u     /* g = 0: plain argmax of l/T (tie tests only)  */
+#define FS_FLAG_STORE_LOGITS 0x2u /* also write f32 logits l (before 1/T) to      \
+                                     out_logits [B, V]: the logits-store flag the  \
+                                     IO-model check uses (Section 3)               */
+
+/* dtype codes of materialised logits Y. */
+#define FS_DTYPE_BF16 0
+#define FS_DTYPE_F32 1
+
+/* Upper limits checked on the host. */
+#define FS_MAX_VOCAB 2147483647LL /* indices are stored as int32 candidates */
+#define FS_MAX_BATCH 16777216LL
+
+/* ---------------------------------------------------------------------------
+ * fs_sample -- the whole hot path: Stage 1 then Stage 2.
+ *   H            device bf16 [B, D], row-major (row stride D elements)
+ *   W            device bf16 [V, D], row-major (row stride D elements)
+ *   temperature  scalar T (used when temperatures == NULL)
+ *   temperatures NULL or device f32 [B]
+ *   seed, offset Philox key word and counter word (see Noise above)
+ *   out_idx      device int64 [B]: sampled token per row (-1: invalid row T)
+ *   out_score    NULL or device f32 [B]: the winning perturbed score s
+ * Candidate workspace: a buffer cached per (device, stream) inside the
+ * library, grown stream-ordered with cudaMallocAsync/cudaFreeAsync.  Calls on
+ * one stream reuse it in order.  fs_release_workspaces() frees the cache.
+ * Returns FS_ERR_NO_MEMORY if the workspace cannot be grown.
+ * ------------------------------------------------------------------------- */
+fs_status fs_sample(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                    float temperature, const float *temperatures, uint64_t seed,
+                    uint64_t offset, int64_t *out_idx, float *out_score, void *stream);
+
+/* Bytes of caller workspace that fs_sample_ex, fs_stage1/fs_stage2 and
+ * fs_sample_from_logits need for (B, V, D) on the current device.
+ * Returns 0 on a bad argument or when no device is visible. */
+size_t fs_workspace_size(int64_t B, int64_t V, int64_t D);
+
+/* ---------------------------------------------------------------------------
+ * fs_sample_ex -- fs_sample with a caller workspace and flags.
+ *   flags       FS_FLAG_NO_NOISE | FS_FLAG_STORE_LOGITS
+ *   out_logits  device f32 [B, V] row-major; required iff FS_FLAG_STORE_LOGITS
+ *               (receives l = H W^T before the temperature; the fused path
+ *               otherwise never materialises it)
+ *   workspace   device buffer of ws_bytes >= fs_workspace_size(B, V, D),
+ *               16-byte aligned; FS_ERR_NO_MEMORY if smaller
+ * ------------------------------------------------------------------------- */
+fs_status fs_sample_ex(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                       float temperature, const float *temperatures, uint64_t seed,
+                       uint64_t offset, uint32_t flags, int64_t *out_idx,
+                       float *out_score, float *out_logits, void *workspace,
+                       size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * The two stages separately (method section, Stage 1 / Stage 2).
+ * fs_stage1 runs the fused GEMM + temperature + Gumbel + tile-argmax kernel
+ * and leaves one (score, index) candidate per (row, candidate slot) in
+ * `workspace`; fs_stage2 reduces them to out_idx / out_score.  Both must be
+ * called with the same (B, V, D) on the same device; fs_stage2 also needs the
+ * temperatures to mark invalid rows.  fs_sample_ex == fs_stage1 + fs_stage2.
+ * Argument meanings as for fs_sample_ex.
+ * ------------------------------------------------------------------------- */
+fs_status fs_stage1(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                    float temperature, const float *temperatures, uint64_t seed,
+                    uint64_t offset, uint32_t flags, float *out_logits,
+                    void *workspace, size_t ws_bytes, void *stream);
+fs_status fs_stage2(int64_t B, int64_t V, int64_t D, float temperature,
+                    const float *temperatures, int64_t *out_idx, float *out_score,
+                    const void *workspace, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Unfused comparator: the baseline the IO model of Section 3 describes, a
+ * GEMM that writes the logits Y to HBM followed by a sampling pass that reads
+ * them back.  Same noise, temperature and tie rule as the fused path.
+ *
+ * fs_logits_gemm        Y = H W^T, written as bf16 or f32 [B, V] row-major.
+ * fs_sample_from_logits Gumbel-max over materialised logits Y [B, V]
+ *                       (bf16 or f32, row-major, row stride V); flags:
+ *                       FS_FLAG_NO_NOISE only.  workspace as fs_sample_ex.
+ * fs_sample_unfused     fs_logits_gemm then fs_sample_from_logits; Y is a
+ *                       caller buffer of B*V elements of y_dtype.
+ * With y_dtype = FS_DTYPE_F32 the unfused path samples exactly what the fused
+ * path samples; with FS_DTYPE_BF16 the logits are rounded to bf16 first.
+ * ------------------------------------------------------------------------- */
+fs_status fs_logits_gemm(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                         void *Y, int y_dtype, void *stream);
+fs_status fs_sample_from_logits(const void *Y, int y_dtype, int64_t B, int64_t V,
+                                float temperature, const float *temperatures,
+                                uint64_t seed, uint64_t offset, uint32_t flags,
+                                int64_t *out_idx, float *out_score, void *workspace,
+                                size_t ws_bytes, void *stream);
+fs_status fs_sample_unfused(const void *H, const void *W, int64_t B, int64_t V,
+                            int64_t D, float temperature, const float *temperatures,
+                            uint64_t seed, uint64_t offset, void *Y, int y_dtype,
+                            int64_t *out_idx, float *out_score, void *workspace,
+                            size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * fs_debug_noise -- test hook: the random word and Gumbel of every element
+ * (b, v) for rows b0 .. b0+nb-1 and vocabulary 0 .. V-1, computed by the
+ * same device functions as the Stage 1 epilogue.
+ *   out_words  NULL or device uint32 [nb, V];  out_g  NULL or device f32 [nb, V]
+ * ------------------------------------------------------------------------- */
+fs_status fs_debug_noise(uint64_t seed, uint64_t offset, int64_t b0, int64_t nb,
+                         int64_t V, uint32_t *out_words, float *out_g, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * fs_get_device_status -- synchronise `stream`, then read and clear the
+ * library's device error word on the current device.  *out_word (may be
+ * NULL) receives the raw bits: 1 = a bounded wait inside a kernel expired.
+ * Returns FS_ERR_TIMEOUT if any bit was set, FS_ERR_CUDA if a CUDA call
+ * failed, FS_OK otherwise.
+ * ------------------------------------------------------------------------- */
+fs_status fs_get_device_status(void *stream, uint32_t *out_word);
+
+/* ---------------------------------------------------------------------------
+ * fs_plan_info -- host-only description of the Stage 1 schedule for
+ * (B, V, D) on a GPU with num_sms SMs; launches nothing and needs no device.
+ *   out[0] batch tiles of 128 rows (nM)       out[1] vocabulary partitions (P)
+ *   out[2] CTAs launched (P * nM)             out[3] candidate slots per row
+ *   out[4] workspace bytes                    out[5] max vocab tiles per CTA
+ * ------------------------------------------------------------------------- */
+fs_status fs_plan_info(int64_t B, int64_t V, int64_t D, int num_sms, int64_t out[6]);
+
+/* Frees every workspace cached by fs_sample (all devices and streams).  The
+ * caller must make sure no fs_sample call is still running on the GPU. */
+fs_status fs_release_workspaces(void);
+
+/* Thread-local text for the last non-FS_OK status of this thread. */
+const char *fs_last_error_string(void);
+
+/* Library version string. */
+const char *fs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FS_SAMPLE_H */

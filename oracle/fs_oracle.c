@@ -223,17 +223,21 @@ static void sample_row(const float *l32, int64_t b, int64_t V, float Tb,
 
 /* Sample one index per row from given f32 logits [B, V] (row-major).
  * T: per-row temperatures [B] (the caller broadcasts a scalar).
+ * row_ids: NULL, or the row index b that each of the B given rows has in the
+ * full batch (it keys the noise counter); NULL means 0..B-1.
  * out_idx [B], out_score [B], out_second [B]; out_scores [B, V] may be NULL. */
 void oracle_sample_from_logits(const float *logits, int64_t B, int64_t V,
-                               const float *T, uint64_t seed, uint64_t offset,
-                               uint32_t flags, int64_t *out_idx, float *out_score,
-                               float *out_second, float *out_scores, int nthreads) {
+                               const float *T, const int64_t *row_ids, uint64_t seed,
+                               uint64_t offset, uint32_t flags, int64_t *out_idx,
+                               float *out_score, float *out_second, float *out_scores,
+                               int nthreads) {
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #endif
     float *s = (float *)malloc(sizeof(float) * (size_t)(V > 0 ? V : 1));
     for (int64_t b = 0; b < B; ++b) {
-        sample_row(logits + b * V, b, V, T[b], seed, offset, flags, s, &out_idx[b],
+        int64_t row = row_ids ? row_ids[b] : b;
+        sample_row(logits + b * V, row, V, T[b], seed, offset, flags, s, &out_idx[b],
                    &out_score[b], &out_second[b]);
         if (out_scores) memcpy(out_scores + b * V, s, sizeof(float) * (size_t)V);
     }
@@ -241,11 +245,12 @@ void oracle_sample_from_logits(const float *logits, int64_t B, int64_t V,
 }
 
 /* The whole hot path from H and W: logits (fp64 sum rounded to f32), then the
- * full Gumbel-max pass.  out_logits [B, V] (fp64, optional) receives the
- * unrounded sums for logits-tolerance checks. */
+ * full Gumbel-max pass.  row_ids as for oracle_sample_from_logits.
+ * out_logits [B, V] (fp64, optional) receives the unrounded sums for
+ * logits-tolerance checks. */
 void oracle_sample(const uint16_t *H, const uint16_t *W, int64_t B, int64_t V,
-                   int64_t D, const float *T, uint64_t seed, uint64_t offset,
-                   uint32_t flags, int64_t *out_idx, float *out_score,
+                   int64_t D, const float *T, const int64_t *row_ids, uint64_t seed,
+                   uint64_t offset, uint32_t flags, int64_t *out_idx, float *out_score,
                    float *out_second, double *out_logits, int nthreads) {
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
@@ -261,7 +266,8 @@ void oracle_sample(const uint16_t *H, const uint16_t *W, int64_t B, int64_t V,
             l32[v] = (float)l64[v];
         }
         if (out_logits) memcpy(out_logits + b * V, l64, sizeof(double) * (size_t)V);
-        sample_row(l32, b, V, T[b], seed, offset, flags, s, &out_idx[b],
+        int64_t row = row_ids ? row_ids[b] : b;
+        sample_row(l32, row, V, T[b], seed, offset, flags, s, &out_idx[b],
                    &out_score[b], &out_second[b]);
     }
     free(l64);

@@ -46,10 +46,10 @@ def _load():
         lib.oracle_gumbel_block.restype = None
         lib.oracle_logits.argtypes = [vp, vp, i64, i64, i64, vp, i32]
         lib.oracle_logits.restype = None
-        lib.oracle_sample_from_logits.argtypes = [vp, i64, i64, vp, u64, u64, u32,
+        lib.oracle_sample_from_logits.argtypes = [vp, i64, i64, vp, vp, u64, u64, u32,
                                                   vp, vp, vp, vp, i32]
         lib.oracle_sample_from_logits.restype = None
-        lib.oracle_sample.argtypes = [vp, vp, i64, i64, i64, vp, u64, u64, u32,
+        lib.oracle_sample.argtypes = [vp, vp, i64, i64, i64, vp, vp, u64, u64, u32,
                                       vp, vp, vp, vp, i32]
         lib.oracle_sample.restype = None
         lib.oracle_num_threads.argtypes = []
@@ -141,27 +141,41 @@ def _temps(T, B):
     return np.ascontiguousarray(T)
 
 
-def sample_from_logits(l32, T, seed, offset, flags=0, want_scores=False, nthreads=0):
+def _rows(row_ids, B):
+    if row_ids is None:
+        return None
+    r = np.ascontiguousarray(row_ids, dtype=np.int64)
+    assert r.shape == (B,)
+    return r
+
+
+def sample_from_logits(l32, T, seed, offset, flags=0, want_scores=False, nthreads=0,
+                       row_ids=None):
     """Full Gumbel-max pass over given f32 logits [B, V].
 
+    row_ids: optional row index (in the full batch) of each given row; it keys
+    the noise counter.  Default 0..B-1.
     Returns (idx int64 [B], best f32 [B], second f32 [B], scores or None).
     """
     L = _c(l32, np.float32)
     B, V = L.shape
     Tv = _temps(T, B)
+    rows = _rows(row_ids, B)
     idx = np.zeros(B, dtype=np.int64)
     best = np.zeros(B, dtype=np.float32)
     second = np.zeros(B, dtype=np.float32)
     scores = np.zeros((B, V), dtype=np.float32) if want_scores else None
-    _load().oracle_sample_from_logits(_ptr(L), B, V, _ptr(Tv), seed, offset, flags,
+    _load().oracle_sample_from_logits(_ptr(L), B, V, _ptr(Tv), _ptr(rows), seed, offset, flags,
                                       _ptr(idx), _ptr(best), _ptr(second),
                                       _ptr(scores), nthreads)
     return idx, best, second, scores
 
 
-def sample(H_bits, W_bits, T, seed, offset, flags=0, want_logits=False, nthreads=0):
+def sample(H_bits, W_bits, T, seed, offset, flags=0, want_logits=False, nthreads=0,
+           row_ids=None):
     """The whole path from bf16 H [B, D] and W [V, D].
 
+    row_ids: optional row index (in the full batch) of each given row of H.
     Returns (idx int64 [B], best f32 [B], second f32 [B], logits64 or None).
     """
     H = _c(H_bits, np.uint16)
@@ -170,11 +184,12 @@ def sample(H_bits, W_bits, T, seed, offset, flags=0, want_logits=False, nthreads
     V, D2 = W.shape
     assert D == D2
     Tv = _temps(T, B)
+    rows = _rows(row_ids, B)
     idx = np.zeros(B, dtype=np.int64)
     best = np.zeros(B, dtype=np.float32)
     second = np.zeros(B, dtype=np.float32)
     l64 = np.zeros((B, V), dtype=np.float64) if want_logits else None
-    _load().oracle_sample(_ptr(H), _ptr(W), B, V, D, _ptr(Tv), seed, offset, flags,
+    _load().oracle_sample(_ptr(H), _ptr(W), B, V, D, _ptr(Tv), _ptr(rows), seed, offset, flags,
                           _ptr(idx), _ptr(best), _ptr(second), _ptr(l64), nthreads)
     return idx, best, second, l64
 

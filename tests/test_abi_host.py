@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The shared library must load, export every function include/fs_sample.h
+declares, describe its schedule, and reject bad arguments with a status and a
+message before touching the GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import exact_sampling_lm_gb300 as fs
+from exact_sampling_lm_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from exact_sampling_lm_gb300 import build
+    build.build()
+
+
+def declared_functions():
+    names = []
+    for fname in sorted(os.listdir(HEADER_DIR)):
+        if not fname.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fname)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(fs_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("fs_sample", "fs_sample_ex", "fs_stage1", "fs_stage2", "fs_workspace_size",
+                 "fs_logits_gemm", "fs_sample_from_logits", "fs_sample_unfused",
+                 "fs_debug_noise", "fs_get_device_status", "fs_last_error_string",
+                 "fs_version", "fs_plan_info", "fs_release_workspaces"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    handle = ctypes.CDLL(_lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(handle, name), name
+        assert name in _lib.SIGNATURES, "binding lacks " + name
+
+
+def test_version_and_error_string():
+    assert "sm_103a" in fs.fs_version()
+    assert isinstance(fs.fs_last_error_string(), str)
+
+
+@pytest.mark.parametrize("B,V,D,sms", [(1, 128256, 4096, 152), (64, 128256, 4096, 152),
+                                       (256, 151936, 3584, 152), (1024, 128256, 8192, 152),
+                                       (512, 262144, 2304, 152), (4, 4096, 256, 152),
+                                       (300, 50257, 72, 148), (3, 5, 8, 152)])
+def test_plan_covers_the_vocabulary(B, V, D, sms):
+    """Partitions are disjoint, cover [0, V) in 16-row units, and every CTA
+    gets at most max_tiles tiles of <= 256 rows; one CTA per SM at most."""
+    p = fs.fs_plan_info(B, V, D, sms)
+    nM = (B + 127) // 128
+    assert p["nM"] == nM
+    assert p["G"] == p["P"] * nM <= max(sms, nM)
+    assert p["nCand"] == 2 * p["P"]
+    U = (V + 15) // 16
+    covered = 0
+    for part in range(p["P"]):
+        u0 = part * U // p["P"]
+        u1 = (part + 1) * U // p["P"]
+        r0, r1 = 16 * u0, min(16 * u1, V)
+        assert r0 == covered
+        covered = r1
+        assert (r1 - r0 + 255) // 256 <= p["max_tiles"]
+        assert r1 > r0
+    assert covered == V
+    slots = max(p["nCand"], (V + 8191) // 8192)
+    assert p["ws_bytes"] >= 8 * slots * B
+
+
+def call_sample(H=16, W=16, B=4, V=64, D=64, T=1.0, temps=None, out=16):
+    return _lib.lib().fs_sample(H, W, B, V, D, T, temps, 0, 0, out, None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(H=None), _lib.FS_ERR_INVALID_ARG),
+    (dict(W=None), _lib.FS_ERR_INVALID_ARG),
+    (dict(out=None), _lib.FS_ERR_INVALID_ARG),
+    (dict(B=0), _lib.FS_ERR_INVALID_ARG),
+    (dict(V=0), _lib.FS_ERR_INVALID_ARG),
+    (dict(D=0), _lib.FS_ERR_INVALID_ARG),
+    (dict(D=12), _lib.FS_ERR_UNSUPPORTED),
+    (dict(H=24), _lib.FS_ERR_UNSUPPORTED),
+    (dict(W=8), _lib.FS_ERR_UNSUPPORTED),
+    (dict(V=2**31), _lib.FS_ERR_UNSUPPORTED),
+    (dict(B=2**24 + 1), _lib.FS_ERR_UNSUPPORTED),
+    (dict(T=0.0), _lib.FS_ERR_INVALID_ARG),
+    (dict(T=-1.0), _lib.FS_ERR_INVALID_ARG),
+    (dict(T=float("inf")), _lib.FS_ERR_INVALID_ARG),
+    (dict(T=float("nan")), _lib.FS_ERR_INVALID_ARG),
+])
+def test_bad_arguments_are_rejected_before_any_launch(kw, status):
+    assert call_sample(**kw) == status
+    assert len(fs.fs_last_error_string()) > 0
+
+
+def test_other_entry_points_validate():
+    L = _lib.lib()
+    assert L.fs_stage1(16, 16, 4, 64, 64, 1.0, None, 0, 0, 0x80, None, 16, 1 << 20, None) \
+        == _lib.FS_ERR_INVALID_ARG  # unknown flag
+    assert L.fs_stage1(16, 16, 4, 64, 64, 1.0, None, 0, 0, _lib.FS_FLAG_STORE_LOGITS, None, 16,
+                       1 << 20, None) == _lib.FS_ERR_INVALID_ARG  # logits buffer missing
+    assert L.fs_logits_gemm(16, 16, 4, 64, 64, 16, 7, None) == _lib.FS_ERR_INVALID_ARG
+    assert L.fs_sample_from_logits(16, 0, 4, 64, 1.0, None, 0, 0, _lib.FS_FLAG_STORE_LOGITS,
+                                   16, None, 16, 1 << 20, None) == _lib.FS_ERR_INVALID_ARG
+    assert L.fs_debug_noise(0, 0, -1, 1, 8, 16, None, None) == _lib.FS_ERR_INVALID_ARG
+    assert L.fs_debug_noise(0, 0, 0, 1, 8, None, None, None) == _lib.FS_ERR_INVALID_ARG
+    out = (ctypes.c_int64 * 6)()
+    assert L.fs_plan_info(4, 64, 64, 0, out) == _lib.FS_ERR_INVALID_ARG
+    assert L.fs_workspace_size(0, 64, 64) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
+def test_valid_call_without_a_device_reports_cuda_error():
+    """With valid arguments but no GPU the call fails with FS_ERR_CUDA (or
+    UNSUPPORTED) instead of crashing: there is no CPU fallback."""
+    st = call_sample()
+    assert st in (_lib.FS_ERR_CUDA, _lib.FS_ERR_UNSUPPORTED)

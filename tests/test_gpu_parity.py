@@ -1,0 +1,286 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars (FlashSampling's exactness claim: the tiled kernel returns the same
+maximizer as a full Gumbel-max pass, Appendix C):
+  * noise words bit-exact; Gumbels within 4 ulp(g) + 1e-6 of the oracle's
+    double-precision value rounded to f32;
+  * logits within |dl| <= 2e-2 of the oracle's fp64 sums (bf16 inputs, f32
+    accumulation in a different order);
+  * sampled indices bit-exact, except where the oracle's two best perturbed
+    scores are closer than 1e-3 (a near-tie, where the f32 rounding of a
+    different summation order may decide); near-ties are counted and printed.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+LOGIT_TOL = 2e-2
+NEAR_TIE = 1e-3
+
+
+@pytest.fixture(scope="module")
+def fs():
+    import exact_sampling_lm_gb300 as fs_mod
+    from exact_sampling_lm_gb300 import build
+    build.build()
+    return fs_mod
+
+
+@pytest.fixture(scope="module")
+def dev():
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+def bits(t):
+    return workloads.to_bits(t)
+
+
+def host_T(T, B):
+    if isinstance(T, torch.Tensor):
+        return T.detach().cpu().numpy().astype(np.float32)
+    return np.full(B, T, dtype=np.float32)
+
+
+def compare_indices(g_idx, o_idx, o_best, o_second, label=""):
+    near = (o_best - o_second) < NEAR_TIE
+    mism = g_idx != o_idx
+    bad = mism & ~near
+    assert not bad.any(), "%s: %d index mismatches away from near-ties at rows %s" % (
+        label, int(bad.sum()), np.nonzero(bad)[0][:10])
+    n_near_mism = int((mism & near).sum())
+    print("[%s] rows=%d near-ties=%d near-tie mismatches=%d" % (label, len(g_idx),
+                                                               int(near.sum()), n_near_mism))
+    return n_near_mism
+
+
+def run_and_check(fs, H, W, T, seed, offset, label, flags=0, store=True, rows=None):
+    """Fused path vs oracle.  rows: subset of rows to check (None = all)."""
+    B, D = H.shape
+    V = W.shape[0]
+    f = flags | (fs.FS_FLAG_STORE_LOGITS if store else 0)
+    idx, score, logits = fs.fs_sample_ex(H, W, temperature=T, seed=seed, offset=offset, flags=f)
+    torch.cuda.synchronize()
+    assert fs.fs_get_device_status() == 0
+    rows = np.arange(B) if rows is None else np.asarray(rows)
+    Hb = bits(H)[rows]
+    Wb = bits(W)
+    Th = host_T(T, B)[rows]
+    o_idx, o_best, o_second, o_l64 = oracle.sample(Hb, Wb, Th, seed, offset,
+                                                   flags=(oracle.NO_NOISE if flags & 1 else 0),
+                                                   want_logits=store, row_ids=rows)
+    g_idx = idx.cpu().numpy()[rows]
+    if store:
+        gl = logits[torch.as_tensor(rows, device=logits.device)].cpu().numpy().astype(np.float64)
+        dl = np.abs(gl - o_l64).max()
+        assert dl <= LOGIT_TOL, "%s: max |dl| = %g" % (label, dl)
+        print("[%s] max |dl| = %.3e" % (label, dl))
+    compare_indices(g_idx, o_idx, o_best, o_second, label)
+    g_score = score.cpu().numpy()[rows]
+    same = g_idx == o_idx
+    valid = same & np.isfinite(o_best)
+    if valid.any():
+        ds = np.abs(g_score[valid] - o_best[valid])
+        lim = LOGIT_TOL / np.minimum(Th[valid], 1.0) + 1e-5
+        assert np.all(ds <= lim), "%s: winning score differs by %g" % (label, ds.max())
+    invalid = ~(np.isfinite(Th) & (Th > 0))
+    assert np.all(g_idx[invalid] == -1) and np.all(np.isnan(g_score[invalid]))
+    return idx, score
+
+
+# ---------------------------------------------------------------- noise
+
+def test_noise_words_bit_exact_and_gumbel_within_bound(fs, dev):
+    for seed, offset, b0, nb, V in [(0x5EED0040, 0, 0, 256, 4099), (2**64 - 1, 2**63, 17, 64, 8192),
+                                    (12345, 7, 1 << 20, 1024, 16384)]:
+        words, g = fs.fs_debug_noise(seed, offset, b0, nb, V)
+        torch.cuda.synchronize()
+        o_words, o_g = oracle.noise_block(seed, offset, b0, nb, 0, V)
+        assert np.array_equal(words.cpu().numpy().view(np.uint32), o_words)
+        gg = g.cpu().numpy().astype(np.float64)
+        og = o_g.astype(np.float64)
+        ulp = np.spacing(np.abs(o_g)).astype(np.float64)
+        err = np.abs(gg - og)
+        assert np.all(err <= 4 * ulp + 1e-6), "max err %g" % err.max()
+        print("noise block %dx%d: max |dg| = %.3e, max in ulps = %.2f" % (
+            nb, V, err.max(), float((err / ulp).max())))
+
+
+# ---------------------------------------------------------------- small exhaustive cases
+
+def test_tiny_workload(fs, dev):
+    B = 4
+    H = workloads.make_hidden("tiny", B).to(dev)
+    W = workloads.make_weights("tiny").to(dev)
+    seed, offset = workloads.sampling_seed("tiny", B)
+    for off in (offset, offset + 1, offset + 12345):
+        run_and_check(fs, H, W, 1.0, seed, off, "tiny off=%d" % off)
+
+
+@pytest.mark.parametrize("B,V,D", [
+    (1, 5, 8), (3, 17, 16), (5, 100, 72), (1, 4096, 256), (7, 4099, 136),
+    (127, 2000, 64), (128, 2048, 128), (129, 3001, 64), (255, 1000, 520),
+    (300, 5003, 200), (2, 50257, 64), (33, 40000, 64), (130, 41000, 96),
+])
+def test_ragged_shapes(fs, dev, B, V, D):
+    """Batch tails (B not a multiple of 128), vocabulary tails (V not a
+    multiple of 16 / 256), partial k-blocks (D not a multiple of 64), several
+    tiles per CTA (V / 152 > 256) and several batch tiles."""
+    g = torch.Generator(device="cpu").manual_seed(B * 7919 + V * 31 + D)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * (1.5 / D ** 0.5)).to(torch.bfloat16).to(dev)
+    run_and_check(fs, H, W, 0.9, 1000 + B, 3, "B=%d V=%d D=%d" % (B, V, D))
+
+
+def test_per_row_temperatures_with_invalid_rows(fs, dev):
+    B, V, D = 40, 3000, 128
+    g = torch.Generator(device="cpu").manual_seed(4)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.1).to(torch.bfloat16).to(dev)
+    T = 0.5 + torch.rand(B, generator=g)
+    T[3] = 0.0
+    T[7] = -1.0
+    T[11] = float("inf")
+    T[19] = float("nan")
+    T[23] = 1e-3
+    T[29] = 1e3
+    run_and_check(fs, H, W, T.to(dev), 77, 1, "per-row T")
+
+
+def test_no_noise_ties_go_to_lowest_index(fs, dev):
+    """Duplicated W rows give exact logit ties; with the noise off the lowest
+    duplicate must win in every tile/partition arrangement."""
+    B, V, D = 16, 20000, 64
+    g = torch.Generator(device="cpu").manual_seed(9)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16)
+    W = (torch.randn((V, D), generator=g) * 0.1).to(torch.bfloat16)
+    l = (H.float() @ W.float().T)
+    top = l.argmax(dim=1)
+    for b in range(B):  # copy each row's winner to several later positions
+        for dst in (int(top[b]) + 1 + 997 * b % 5000, V - 1 - b):
+            if dst < V and dst > int(top[b]):
+                W[dst] = W[top[b]]
+    idx, _ = run_and_check(fs, H.to(dev), W.to(dev), 1.0, 0, 0, "no-noise ties",
+                           flags=fs.FS_FLAG_NO_NOISE)
+
+
+def test_bigvocab_duplicates_small(fs, dev):
+    B, V, D = 8, 26214, 64
+    W = workloads.make_weights("bigvocab", V=V, D=D).to(dev)
+    H = workloads.make_hidden("bigvocab", B, D=D).to(dev)
+    run_and_check(fs, H, W, 1.0, 5, 0, "bigvocab-small noise")
+    run_and_check(fs, H, W, 1.0, 5, 0, "bigvocab-small no-noise", flags=fs.FS_FLAG_NO_NOISE)
+
+
+# ---------------------------------------------------------------- API consistency
+
+def test_entry_points_agree_and_are_deterministic(fs, dev):
+    B, V, D = 70, 30011, 192
+    g = torch.Generator(device="cpu").manual_seed(21)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.08).to(torch.bfloat16).to(dev)
+    T = (0.5 + torch.rand(B, generator=g)).to(dev)
+    i1, s1 = fs.fs_sample(H, W, temperature=T, seed=3, offset=9)
+    i2, s2, _ = fs.fs_sample_ex(H, W, temperature=T, seed=3, offset=9)
+    ws = fs.workspace(B, V, D)
+    fs.fs_stage1(H, W, ws, temperature=T, seed=3, offset=9)
+    i3 = torch.empty(B, dtype=torch.int64, device=dev)
+    s3 = torch.empty(B, dtype=torch.float32, device=dev)
+    fs.fs_stage2(B, V, D, ws, temperature=T, out_idx=i3, out_score=s3)
+    i4, s4, _ = fs.fs_sample_ex(H, W, temperature=T, seed=3, offset=9,
+                                flags=fs.FS_FLAG_STORE_LOGITS)
+    torch.cuda.synchronize()
+    for i, s in ((i2, s2), (i3, s3), (i4, s4)):
+        assert torch.equal(i1, i) and torch.equal(s1, s)
+    # another offset changes the draw
+    i5, _ = fs.fs_sample(H, W, temperature=T, seed=3, offset=10)
+    assert not torch.equal(i1, i5)
+
+
+def test_side_stream_and_workspace_growth(fs, dev):
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for B in (2, 300, 5):
+            g = torch.Generator(device="cpu").manual_seed(B)
+            H = torch.randn((B, 64), generator=g).to(torch.bfloat16).to(dev)
+            W = (torch.randn((9000, 64), generator=g) * 0.1).to(torch.bfloat16).to(dev)
+            outs.append((H, W, fs.fs_sample(H, W, temperature=1.0, seed=1, offset=2)))
+    s.synchronize()
+    for H, W, (idx, score) in outs:
+        ref, _ = fs.fs_sample(H, W, temperature=1.0, seed=1, offset=2)
+        assert torch.equal(idx, ref)
+
+
+# ---------------------------------------------------------------- unfused comparator
+
+def test_unfused_f32_equals_fused(fs, dev):
+    B, V, D = 65, 33000, 256
+    g = torch.Generator(device="cpu").manual_seed(5)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.08).to(torch.bfloat16).to(dev)
+    fi, fsc, fl = fs.fs_sample_ex(H, W, temperature=0.8, seed=8, offset=1,
+                                  flags=fs.FS_FLAG_STORE_LOGITS)
+    ui, usc, Y = fs.fs_sample_unfused(H, W, temperature=0.8, seed=8, offset=1,
+                                      y_dtype=fs.FS_DTYPE_F32)
+    torch.cuda.synchronize()
+    assert torch.equal(Y, fl)
+    assert torch.equal(fi, ui) and torch.equal(fsc, usc)
+
+
+def test_unfused_bf16_logits(fs, dev):
+    B, V, D = 9, 12345, 128
+    g = torch.Generator(device="cpu").manual_seed(6)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.1).to(torch.bfloat16).to(dev)
+    Y16 = fs.fs_logits_gemm(H, W, y_dtype=fs.FS_DTYPE_BF16)
+    Y32 = fs.fs_logits_gemm(H, W, y_dtype=fs.FS_DTYPE_F32)
+    torch.cuda.synchronize()
+    o = oracle.logits(bits(H), bits(W))
+    assert np.abs(Y32.cpu().numpy() - o).max() <= LOGIT_TOL
+    y16 = Y16.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(y16 - o) <= LOGIT_TOL + np.abs(o) * 2.0 ** -8)
+    assert torch.equal(Y16, Y32.to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("B,V", [(1, 7), (6, 8193), (33, 50000)])
+def test_sample_from_materialised_logits(fs, dev, dtype, B, V):
+    """The unfused sampling pass on seeded synthetic logits vs the oracle's
+    full pass over the same logits."""
+    g = torch.Generator(device="cpu").manual_seed(B * 13 + V)
+    Y = (2.0 * torch.randn((B, V), generator=g)).to(dtype)
+    T = (0.5 + torch.rand(B, generator=g))
+    idx, score = fs.fs_sample_from_logits(Y.to(dev), temperature=T.to(dev), seed=42, offset=3)
+    torch.cuda.synchronize()
+    o_idx, o_best, o_second, _ = oracle.sample_from_logits(Y.float().numpy(), T.numpy(), 42, 3)
+    compare_indices(idx.cpu().numpy(), o_idx, o_best, o_second, "logits %s B=%d V=%d" % (dtype, B, V))
+    same = idx.cpu().numpy() == o_idx
+    assert np.all(np.abs(score.cpu().numpy()[same] - o_best[same]) <= 4e-6 * np.abs(o_best[same]) + 2e-6)
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+FULL = [("llama3_8b", 64), ("llama3_8b", 1), ("qwen", 256), ("qwen", 100),
+        ("llama3_70b", 1024), ("bigvocab", 512), ("bigvocab", 1)]
+
+
+@pytest.mark.parametrize("name,B", FULL)
+def test_full_size_sampled_rows(fs, dev, name, B):
+    """Each workload at full size, in the launch configuration the benchmark
+    times; the oracle checks a sample of rows (first, last, and spread)."""
+    W = workloads.make_weights(name, device=dev)
+    H = workloads.make_hidden(name, B, device=dev)
+    T = workloads.make_temperature(name, B, device=dev)
+    seed, offset = workloads.sampling_seed(name, B)
+    rows = sorted(set([0, B - 1] + list(range(0, B, max(1, B // 6)))))[:8]
+    run_and_check(fs, H, W, T, seed, offset, "%s B=%d" % (name, B), rows=rows)
+    if name == "bigvocab":
+        run_and_check(fs, H, W, T, seed, offset, "%s B=%d no-noise" % (name, B),
+                      flags=fs.FS_FLAG_NO_NOISE, store=False, rows=rows)

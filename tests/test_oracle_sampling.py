@@ -226,3 +226,18 @@ def test_gumbel_max_law_by_quadrature():
         f = lambda x: pdf(x - l[i]) * np.prod([cdf(x - l[j]) for j in range(len(l)) if j != i])
         p, _ = scipy.integrate.quad(f, -20, 40, limit=200)
         assert abs(p - scipy.special.softmax(l)[i]) < 1e-8
+
+
+def test_row_ids_key_the_noise_like_the_full_batch():
+    """Sampling a subset of rows with their batch indices reproduces the
+    full-batch result for those rows (used for sampled-row parity checks)."""
+    rng = np.random.default_rng(12)
+    B, V, D = 9, 70, 24
+    H = bf16_bits(rng.standard_normal((B, D)))
+    W = bf16_bits(0.2 * rng.standard_normal((V, D)))
+    T = rng.uniform(0.5, 1.5, size=B).astype(np.float32)
+    full = oracle.sample(H, W, T, 5, 6)
+    rows = np.array([7, 2, 8])
+    sub = oracle.sample(H[rows], W, T[rows], 5, 6, row_ids=rows)
+    for a, b in zip(full[:3], sub[:3]):
+        assert np.array_equal(a[rows], b)
