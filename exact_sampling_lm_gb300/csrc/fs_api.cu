@@ -57,8 +57,11 @@ bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *p) {
     p->P = static_cast<int>(P);
     p->G = static_cast<int>(P * nM);
     p->nCand = static_cast<int>(2 * P);
+    // tiles of the largest partition: 256-row tiles, then a final 2-unit tile
     const int64_t max_units = (U + P - 1) / P;
-    p->maxTiles = static_cast<int>((max_units * kUnitRows + kBN - 1) / kBN);
+    p->maxTiles = max_units <= 2
+                      ? 1
+                      : static_cast<int>(((max_units - 2) * kUnitRows + kBN - 1) / kBN + 1);
     p->nChunks = static_cast<int>((V + kLogitsChunk - 1) / kLogitsChunk);
     const int64_t slots = p->nCand > p->nChunks ? p->nCand : p->nChunks;
     const int64_t region = ((slots * B * 4) + 255) / 256 * 256;
@@ -210,7 +213,11 @@ static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &
                             cudaStream_t stream) {
     CUtensorMap tmH, tmW64, tmW16;
     fs_status st;
-    if ((st = make_tmap(&tmH, H, p.B, p.D, kBM)) != FS_OK) return st;
+    // With one batch tile, load only the live rows of H (rounded up to the
+    // 8-row swizzle atom); the MMA's other A rows feed TMEM lanes that the
+    // epilogue never reads.
+    const int h_box_rows = p.nM == 1 ? static_cast<int>((p.B + 7) / 8 * 8) : kBM;
+    if ((st = make_tmap(&tmH, H, p.B, p.D, static_cast<uint32_t>(h_box_rows))) != FS_OK) return st;
     if ((st = make_tmap(&tmW64, W, p.V, p.D, 64)) != FS_OK) return st;
     if ((st = make_tmap(&tmW16, W, p.V, p.D, 16)) != FS_OK) return st;
     Stage1Args a;
@@ -233,6 +240,7 @@ static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &
     const bool f32 = (mode == kModeSampleStore) || (mode == kModeGemmF32 && y_dtype == FS_DTYPE_F32);
     a.y_vec_ok = dst && (reinterpret_cast<uintptr_t>(dst) % 16 == 0) &&
                  (f32 ? (p.V % 4 == 0) : (p.V % 8 == 0));
+    a.h_box_rows = h_box_rows;
     a.timeout_ns = wait_timeout_ns();
     cudaError_t e = launch_stage1(mode, tmH, tmW64, tmW16, a, p.G, stream);
     if (e != cudaSuccess) return cuda_fail(e, "Stage 1 launch");

@@ -66,6 +66,7 @@ struct Stage1Args {
     float *out_logits;  // [B][V] f32 (kModeSampleStore)
     void *out_y;        // [B][V] bf16/f32 (GEMM modes)
     int y_vec_ok;       // row starts of Y / out_logits are 16-byte aligned
+    int h_box_rows;     // rows of the H tensor-map box (8..128; rows above are not loaded)
     uint64_t timeout_ns;
 };
 

@@ -14,51 +14,82 @@
 
 namespace fs {
 
-struct Philox4x64Out {
-    uint64_t w[4];
+constexpr uint64_t kPhiloxMul0 = 0xD2E7470EE14C6C93ull;
+constexpr uint64_t kPhiloxMul1 = 0xCA5A826395121157ull;
+constexpr uint64_t kPhiloxWeyl0 = 0x9E3779B97F4A7C15ull;
+constexpr uint64_t kPhiloxWeyl1 = 0xBB67AE8584CAA73Bull;
+
+// One round of the 4x64 Philox bijection: the two 64x64->128 products of
+// words 0 and 2 with the round multipliers; the high halves are xored with
+// words 1 / 3 and the round key; the low halves move to words 3 / 1.
+__device__ __forceinline__ void philox_round(uint64_t &c0, uint64_t &c1, uint64_t &c2,
+                                             uint64_t &c3, uint64_t k0, uint64_t k1) {
+    const uint64_t lo0 = kPhiloxMul0 * c0;
+    const uint64_t hi0 = __umul64hi(kPhiloxMul0, c0);
+    const uint64_t lo1 = kPhiloxMul1 * c2;
+    const uint64_t hi1 = __umul64hi(kPhiloxMul1, c2);
+    c0 = hi1 ^ c1 ^ k0;
+    c1 = lo1;
+    c2 = hi0 ^ c3 ^ k1;
+    c3 = lo0;
+}
+
+// Per-row constants of the counter (v >> 3, b, offset, 0): the product of
+// word 2 (= offset) in round 1 and, through it, the product of word 0 in
+// round 2 do not depend on v.  Precomputing them saves 2 of the 20 products
+// of every call; the result is bit-identical to the plain ten rounds.
+struct PhiloxRow {
+    uint64_t seed;
+    uint64_t r1_c0_part;  // round 1: hi(M1*offset) ^ b ^ k0   (new word 0)
+    uint64_t r1_c1;       // round 1: lo(M1*offset)            (new word 1)
+    uint64_t r2_hi0;      // round 2: hi(M0 * new word 0)
+    uint64_t r2_lo0;      // round 2: lo(M0 * new word 0)      (new word 3)
 };
 
-// Ten rounds of the 4x64 Philox bijection.  Per round: the two 64x64->128
-// products of words 0 and 2 with the round multipliers; the high halves are
-// xored with words 1 / 3 and the round key; the low halves move to words 3 / 1.
-// The key advances by the two Weyl increments between rounds.
-__device__ __forceinline__ Philox4x64Out philox4x64_10(uint64_t c0, uint64_t c1, uint64_t c2,
-                                                      uint64_t c3, uint64_t k0, uint64_t k1) {
-    constexpr uint64_t kMul0 = 0xD2E7470EE14C6C93ull;
-    constexpr uint64_t kMul1 = 0xCA5A826395121157ull;
-    constexpr uint64_t kWeyl0 = 0x9E3779B97F4A7C15ull;
-    constexpr uint64_t kWeyl1 = 0xBB67AE8584CAA73Bull;
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        const uint64_t lo0 = kMul0 * c0;
-        const uint64_t hi0 = __umul64hi(kMul0, c0);
-        const uint64_t lo1 = kMul1 * c2;
-        const uint64_t hi1 = __umul64hi(kMul1, c2);
+__device__ __forceinline__ PhiloxRow philox_row(uint64_t seed, uint64_t offset, uint64_t b) {
+    PhiloxRow r;
+    r.seed = seed;
+    const uint64_t lo1 = kPhiloxMul1 * offset;
+    const uint64_t hi1 = __umul64hi(kPhiloxMul1, offset);
+    r.r1_c0_part = hi1 ^ b ^ seed;  // key word 0 of round 1 is the seed
+    r.r1_c1 = lo1;
+    r.r2_hi0 = __umul64hi(kPhiloxMul0, r.r1_c0_part);
+    r.r2_lo0 = kPhiloxMul0 * r.r1_c0_part;
+    return r;
+}
+
+// The eight 32-bit draws of vocabulary indices 8*v8 .. 8*v8+7 of the row.
+__device__ __forceinline__ void noise_words8(const PhiloxRow &row, uint64_t v8,
+                                             uint32_t (&x)[8]) {
+    // round 1 (key seed, 0): word 0 = v8 varies, word 2 = offset is per row
+    const uint64_t lo0 = kPhiloxMul0 * v8;
+    const uint64_t hi0 = __umul64hi(kPhiloxMul0, v8);
+    uint64_t c0 = row.r1_c0_part;
+    uint64_t c1 = row.r1_c1;
+    uint64_t c2 = hi0;  // ^ word 3 (0) ^ key word 1 (0)
+    uint64_t c3 = lo0;
+    // round 2 (key + Weyl): word 0's product is per row
+    {
+        const uint64_t k0 = row.seed + kPhiloxWeyl0;
+        const uint64_t k1 = kPhiloxWeyl1;
+        const uint64_t lo1 = kPhiloxMul1 * c2;
+        const uint64_t hi1 = __umul64hi(kPhiloxMul1, c2);
         const uint64_t n0 = hi1 ^ c1 ^ k0;
-        const uint64_t n2 = hi0 ^ c3 ^ k1;
+        const uint64_t n2 = row.r2_hi0 ^ c3 ^ k1;
         c0 = n0;
         c1 = lo1;
         c2 = n2;
-        c3 = lo0;
-        k0 += kWeyl0;
-        k1 += kWeyl1;
+        c3 = row.r2_lo0;
     }
-    Philox4x64Out o;
-    o.w[0] = c0;
-    o.w[1] = c1;
-    o.w[2] = c2;
-    o.w[3] = c3;
-    return o;
-}
-
-// The eight 32-bit draws of vocabulary indices v8*8 .. v8*8+7 of row b.
-__device__ __forceinline__ void noise_words8(uint64_t seed, uint64_t offset, uint64_t b,
-                                             uint64_t v8, uint32_t (&x)[8]) {
-    const Philox4x64Out o = philox4x64_10(v8, b, offset, 0ull, seed, 0ull);
+#pragma unroll
+    for (int r = 2; r < 10; ++r)
+        philox_round(c0, c1, c2, c3, row.seed + kPhiloxWeyl0 * static_cast<uint64_t>(r),
+                     kPhiloxWeyl1 * static_cast<uint64_t>(r));
+    const uint64_t w[4] = {c0, c1, c2, c3};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        x[2 * j] = static_cast<uint32_t>(o.w[j]);
-        x[2 * j + 1] = static_cast<uint32_t>(o.w[j] >> 32);
+        x[2 * j] = static_cast<uint32_t>(w[j]);
+        x[2 * j + 1] = static_cast<uint32_t>(w[j] >> 32);
     }
 }
 
@@ -75,6 +106,33 @@ __device__ __forceinline__ float gumbel_from_word(uint32_t x) {
     const float u = uniform_from_word(x);
     const float e = -logf(u);
     return -logf(e);
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Screening threshold of the argmax.  An element with transformed logit lt
+// can only beat the running best `best` if its Gumbel exceeds d = best - lt,
+// i.e. if u > F(d) = exp(-exp(-d)) (Gumbel CDF).  This returns a value that
+// is never above exp(-exp(kScreenSlack - d)) <= F(d - kScreenSlack): the
+// slack absorbs the f32 roundings of d, of s = lt + g and of the computed g,
+// and the factor (1 - 2^-12) absorbs the relative error of the two nested
+// hardware exp2 approximations (about e1 * 1.8e-6 + 2.4e-7 for e1 =
+// exp(slack - d); below 2^-12 for every e1 <= 133, and for larger e1 the
+// true threshold is under 2^-190, far below the smallest u = 2^-24).  Elements with u <= threshold cannot win and
+// skip the two accurate logarithms; the others take the exact path, so the
+// result equals the unscreened scan.  Non-finite cases: best = -inf gives 0
+// (always exact path); NaN d gives NaN (comparison false: such an element
+// cannot win either).
+constexpr float kScreenSlack = 0x1p-10f;
+__device__ __forceinline__ float screen_threshold(float d) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float e1 = ex2_approx(__fmul_rn(kLog2e, kScreenSlack - d));  // exp(slack - d)
+    const float thr = ex2_approx(-kLog2e * e1);                           // exp(-e1)
+    return thr * (1.0f - 0x1p-12f);
 }
 
 }  // namespace fs

@@ -12,6 +12,7 @@
 
 #include "fs_internal.h"
 #include "fs_noise.cuh"
+#include "fs_ptx.cuh"
 
 namespace fs {
 
@@ -46,6 +47,8 @@ __global__ void __launch_bounds__(kStage2Warps * 32)
     stage2_kernel(const float *__restrict__ cand_score, const int32_t *__restrict__ cand_idx,
                   int nCand, int64_t B, const float *__restrict__ temps, float temp_scalar,
                   int64_t *__restrict__ out_idx, float *__restrict__ out_score) {
+    // Launched with programmatic serialization: wait for the producing grid.
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t b = static_cast<int64_t>(blockIdx.x) * kStage2Warps + (threadIdx.x >> 5);
     if (b >= B) return;
@@ -72,9 +75,20 @@ cudaError_t launch_stage2(const float *cand_score, const int32_t *cand_idx, int 
                           int64_t B, const float *temps, float temp_scalar, int64_t *out_idx,
                           float *out_score, cudaStream_t stream) {
     const int64_t blocks = (B + kStage2Warps - 1) / kStage2Warps;
-    stage2_kernel<<<static_cast<unsigned>(blocks), kStage2Warps * 32, 0, stream>>>(
-        cand_score, cand_idx, nCand, B, temps, temp_scalar, out_idx, out_score);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the blocks may be scheduled while the
+    // producing kernel finishes; griddep_wait() orders the reads.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kStage2Warps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, stage2_kernel, cand_score, cand_idx, nCand, B, temps,
+                              temp_scalar, out_idx, out_score);
 }
 
 // ------------------------------------------------------------------ unfused sampling pass
@@ -133,6 +147,7 @@ __global__ void __launch_bounds__(kLogitsThreads)
         const int64_t v_begin = static_cast<int64_t>(chunk) * kLogitsChunk;
         const int64_t v_end = min(V, v_begin + kLogitsChunk);
         const T *row = Y + b * V;
+        const PhiloxRow prow = philox_row(seed, offset, static_cast<uint64_t>(b));
         float best = -INFINITY;
         uint32_t bi = 0xFFFFFFFFu;
         if (t_ok) {
@@ -140,8 +155,7 @@ __global__ void __launch_bounds__(kLogitsThreads)
                 float l[8];
                 load8<T>(row, v, v_end, vec_ok, l);
                 uint32_t x[8];
-                if (!no_noise) noise_words8(seed, offset, static_cast<uint64_t>(b),
-                                            static_cast<uint64_t>(v) >> 3, x);
+                if (!no_noise) noise_words8(prow, static_cast<uint64_t>(v) >> 3, x);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float g = no_noise ? 0.0f : gumbel_from_word(x[e]);
@@ -204,7 +218,8 @@ __global__ void debug_noise_kernel(uint64_t seed, uint64_t offset, int64_t b0, i
         const int64_t rb = i / groups;
         const int64_t v8 = i % groups;
         uint32_t x[8];
-        noise_words8(seed, offset, static_cast<uint64_t>(b0 + rb), static_cast<uint64_t>(v8), x);
+        noise_words8(philox_row(seed, offset, static_cast<uint64_t>(b0 + rb)),
+                     static_cast<uint64_t>(v8), x);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int64_t v = v8 * 8 + e;

@@ -24,7 +24,13 @@
 // the 8-wide Philox block both fall out without cross-thread exchange.
 // CTA c works on batch tile c % nM and vocabulary partition c / nM
 // (partitions are balanced in 16-row units), and writes one candidate per
-// (row, partition, column half).
+// (row, partition, column half).  A partition is cut into 256-row tiles plus
+// a final 32-row tile, so that the one epilogue that cannot overlap an MMA
+// (the last) is short.  Each CTA starts its K loop at a different k-block,
+// so the CTAs do not all request the same H line from L2 at once.
+// The epilogue screens every element with a cheap conservative bound
+// (screen_threshold): only elements that may beat the running best pay for
+// the two accurate logarithms, and the result equals the unscreened scan.
 //
 // Every wait is bounded: on expiry the CTA raises the device error word,
 // tells its other warps to stop, drains its own TMA loads and MMAs, frees TMEM
@@ -46,34 +52,72 @@ constexpr uint32_t kStatusTimeout = 1u;
 
 __device__ __forceinline__ int round_up16(int x) { return (x + 15) & ~15; }
 
+// Rows [r0, r1) of a partition of nu 16-row units: 256-row tiles over the
+// first nu - 2 units, then one final tile over the last two units (fewer if
+// the partition is that small).  Tile starts are multiples of 16 rows.
+struct PartGeom {
+    int r0, r1, nu, nmain, ntiles;
+};
+
+__device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V) {
+    PartGeom g;
+    g.r0 = static_cast<int>(u0 * kUnitRows);
+    g.r1 = static_cast<int>(min(u1 * kUnitRows, static_cast<int64_t>(V)));
+    g.nu = static_cast<int>(u1 - u0);
+    if (g.nu <= 2) {
+        g.nmain = 0;
+        g.ntiles = (g.r1 > g.r0) ? 1 : 0;
+    } else {
+        g.nmain = (kUnitRows * (g.nu - 2) + kBN - 1) / kBN;
+        g.ntiles = g.nmain + 1;
+    }
+    return g;
+}
+
+__device__ __forceinline__ void tile_geom(const PartGeom &g, int t, int &v0, int &tn) {
+    if (g.nu <= 2) {
+        v0 = g.r0;
+        tn = g.r1 - g.r0;
+        return;
+    }
+    const int main_rows = kUnitRows * (g.nu - 2);
+    if (t < g.nmain) {
+        v0 = g.r0 + kBN * t;
+        tn = min(kBN, main_rows - kBN * t);
+    } else {
+        v0 = g.r0 + main_rows;
+        tn = g.r1 - v0;
+    }
+}
+
 __device__ __forceinline__ void raise_timeout(volatile int *abort_flag) {
     atomicOr(&g_status_word, kStatusTimeout);
     *abort_flag = 1;
 }
 
-// Stores n (<= 32) consecutive f32 values of one row.
-__device__ __forceinline__ void store_f32_chunk(float *dst, int n, const uint32_t (&r)[32],
+// Stores n (<= 16) consecutive f32 values of one row.
+__device__ __forceinline__ void store_f32_chunk(float *dst, int n, const uint32_t (&r)[16],
                                                 bool vec_ok) {
-    if (vec_ok && n == 32) {
+    if (vec_ok && n == 16) {
         float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 4; ++i)
             d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 16; ++i)
             if (i < n) dst[i] = __uint_as_float(r[i]);
     }
 }
 
-// Stores n (<= 32) consecutive values of one row rounded to bf16.
+// Stores n (<= 16) consecutive values of one row rounded to bf16.
 __device__ __forceinline__ void store_bf16_chunk(__nv_bfloat16 *dst, int n,
-                                                 const uint32_t (&r)[32], bool vec_ok) {
-    if (vec_ok && n == 32) {
+                                                 const uint32_t (&r)[16], bool vec_ok) {
+    if (vec_ok && n == 16) {
         uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             uint32_t p[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -85,7 +129,7 @@ __device__ __forceinline__ void store_bf16_chunk(__nv_bfloat16 *dst, int n,
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 16; ++i)
             if (i < n) dst[i] = __float2bfloat16_rn(__uint_as_float(r[i]));
     }
 }
@@ -116,12 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int m = blockIdx.x % a.nM;
     const int part = blockIdx.x / a.nM;
-    const int64_t u0 = static_cast<int64_t>(part) * a.U / a.P;
-    const int64_t u1 = static_cast<int64_t>(part + 1) * a.U / a.P;
-    const int r0 = static_cast<int>(u0 * kUnitRows);
-    const int r1 = static_cast<int>(min(u1 * kUnitRows, static_cast<int64_t>(a.V)));
-    const int ntiles = (r1 > r0) ? (r1 - r0 + kBN - 1) / kBN : 0;
+    const PartGeom geom = part_geom(static_cast<int64_t>(part) * a.U / a.P,
+                                    static_cast<int64_t>(part + 1) * a.U / a.P, a.V);
+    const int ntiles = geom.ntiles;
     const int nk = (a.D + kBK - 1) / kBK;
+    const int kb_first = static_cast<int>(blockIdx.x % static_cast<unsigned>(nk));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -144,6 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Stage 2 (launched with programmatic serialization) may be scheduled now;
+    // it waits for this grid's completion before reading the candidates.
+    griddep_launch_dependents();
 
     if (warp == kWarpTma) {
         // ------------------------------------------------ TMA producer
@@ -153,18 +199,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmW16);
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_h = l2_policy_evict_last();
+            const uint32_t h_bytes = static_cast<uint32_t>(a.h_box_rows) * (kBK * 2);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0;      // stages that received at least one load
             uint32_t last_phase_bits = 0;  // phase of the last load per stage
             bool ok = true;
             for (int t = 0; t < ntiles && ok; ++t) {
-                const int v0 = r0 + t * kBN;
-                const int tn16 = round_up16(min(kBN, r1 - v0));
+                int v0, tn;
+                tile_geom(geom, t, v0, tn);
+                const int tn16 = round_up16(tn);
                 const int n64 = tn16 >> 6;
                 const int n16 = (tn16 & 63) >> 4;
-                const uint32_t bytes = kABytes + tn16 * (kBK * 2);
-                for (int kb = 0; kb < nk; ++kb) {
+                const uint32_t bytes = h_bytes + tn16 * (kBK * 2);
+                int kb = kb_first;
+                for (int j = 0; j < nk; ++j) {
                     if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, a.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
@@ -174,18 +223,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *dB = sB + stage * kBBytes;
                     const int kx = kb * kBK;
                     tma_load_2d(dA, &tmH, &full_bar[stage], kx, m * kBM, pol_h);
-                    for (int j = 0; j < n64; ++j)
-                        tma_load_2d(dB + j * 64 * (kBK * 2), &tmW64, &full_bar[stage], kx,
-                                    v0 + j * 64, pol_w);
-                    for (int j = 0; j < n16; ++j)
-                        tma_load_2d(dB + (n64 * 64 + j * 16) * (kBK * 2), &tmW16, &full_bar[stage],
-                                    kx, v0 + n64 * 64 + j * 16, pol_w);
+                    for (int i = 0; i < n64; ++i)
+                        tma_load_2d(dB + i * 64 * (kBK * 2), &tmW64, &full_bar[stage], kx,
+                                    v0 + i * 64, pol_w);
+                    for (int i = 0; i < n16; ++i)
+                        tma_load_2d(dB + (n64 * 64 + i * 16) * (kBK * 2), &tmW16, &full_bar[stage],
+                                    kx, v0 + n64 * 64 + i * 16, pol_w);
                     issued_mask |= 1u << stage;
                     last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if (++kb == nk) kb = 0;
                 }
             }
             if (!ok) raise_timeout(abort_flag);
@@ -210,11 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const int v0 = r0 + t * kBN;
-                const int tn16 = round_up16(min(kBN, r1 - v0));
-                const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(tn16));
+                int v0, tn;
+                tile_geom(geom, t, v0, tn);
+                const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(round_up16(tn)));
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int j = 0; j < nk; ++j) {
                     if (!mbar_wait_bounded(&full_bar[stage], phase, a.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
@@ -226,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
                         umma_bf16_ss(d_tmem, sw128_kmajor_desc(a_addr + ks * kUmmaK * 2),
                                      sw128_kmajor_desc(b_addr + ks * kUmmaK * 2), idesc,
-                                     (kb | ks) != 0 ? 1u : 0u);
+                                     (j | ks) != 0 ? 1u : 0u);
                     }
                     umma_commit(&empty_bar[stage]);
                     if (++stage == kStages) {
@@ -257,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             invT = __frcp_rn(T);
         }
         const bool no_noise = (a.flags & 1u) != 0;
+        const PhiloxRow prow = philox_row(a.seed, a.offset, static_cast<uint64_t>(b));
         float best = -INFINITY;
         int bidx = -1;
         bool ok = true;
@@ -268,36 +319,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            const int v0 = r0 + t * kBN;
-            const int tn = min(kBN, r1 - v0);
-            const int c_lo = h * (kBN / 2);
-            const int c_hi = min(c_lo + kBN / 2, tn);
+            int v0, tn;
+            tile_geom(geom, t, v0, tn);
+            // Columns split between the two halves in 16-column steps.
+            const int cs = min(tn, round_up16((tn + 1) >> 1));
+            const int c_lo = h ? cs : 0;
+            const int c_hi = h ? tn : cs;
             if (warp_has_rows) {
-                for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32_wait(tmem_base + static_cast<uint32_t>(acc * kBN + c0) +
+                for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16_wait(tmem_base + static_cast<uint32_t>(acc * kBN + c0) +
                                        (static_cast<uint32_t>(q * 32) << 16),
                                    r);
-                    const int n_valid = min(32, tn - c0);
+                    const int n_valid = min(16, c_hi - c0);
                     const int vbase = v0 + c0;
                     if (kSample) {
                         if (row_ok && t_ok) {
 #pragma unroll
-                            for (int g8 = 0; g8 < 4; ++g8) {
+                            for (int g8 = 0; g8 < 2; ++g8) {
                                 if (g8 * 8 < n_valid) {
-                                    uint32_t x[8];
-                                    if (!no_noise)
-                                        noise_words8(a.seed, a.offset, static_cast<uint64_t>(b),
-                                                     static_cast<uint64_t>(vbase + g8 * 8) >> 3, x);
+                                    if (no_noise) {
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e) {
-                                        const int i = g8 * 8 + e;
-                                        const float l = __uint_as_float(r[i]);
-                                        const float g = no_noise ? 0.0f : gumbel_from_word(x[e]);
-                                        const float s = __fadd_rn(__fmul_rn(l, invT), g);
-                                        if (i < n_valid && s > best) {
-                                            best = s;
-                                            bidx = vbase + i;
+                                        for (int e = 0; e < 8; ++e) {
+                                            const int i = g8 * 8 + e;
+                                            const float s = __fmul_rn(__uint_as_float(r[i]), invT);
+                                            if (i < n_valid && s > best) {
+                                                best = s;
+                                                bidx = vbase + i;
+                                            }
+                                        }
+                                    } else {
+                                        uint32_t x[8];
+                                        noise_words8(prow, static_cast<uint64_t>(vbase + g8 * 8) >> 3, x);
+                                        // Screen the 8 elements against the best
+                                        // known before the group (a lower bound of
+                                        // the running best, so still conservative),
+                                        // then scan the survivors exactly, in order.
+                                        const float best0 = best;
+                                        float lt[8];
+                                        bool pass[8];
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e) {
+                                            const int i = g8 * 8 + e;
+                                            lt[e] = __fmul_rn(__uint_as_float(r[i]), invT);
+                                            pass[e] = (i < n_valid) &&
+                                                      (uniform_from_word(x[e]) >
+                                                       screen_threshold(best0 - lt[e]));
+                                        }
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e) {
+                                            if (pass[e]) {
+                                                const float s =
+                                                    __fadd_rn(lt[e], gumbel_from_word(x[e]));
+                                                if (s > best) {
+                                                    best = s;
+                                                    bidx = vbase + g8 * 8 + e;
+                                                }
+                                            }
                                         }
                                     }
                                 }

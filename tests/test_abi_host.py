@@ -62,7 +62,8 @@ def test_version_and_error_string():
                                        (300, 50257, 72, 148), (3, 5, 8, 152)])
 def test_plan_covers_the_vocabulary(B, V, D, sms):
     """Partitions are disjoint, cover [0, V) in 16-row units, and every CTA
-    gets at most max_tiles tiles of <= 256 rows; one CTA per SM at most."""
+    gets at most max_tiles tiles (256-row tiles, then a final tile of the last
+    two units); one CTA per SM at most."""
     p = fs.fs_plan_info(B, V, D, sms)
     nM = (B + 127) // 128
     assert p["nM"] == nM
@@ -76,7 +77,9 @@ def test_plan_covers_the_vocabulary(B, V, D, sms):
         r0, r1 = 16 * u0, min(16 * u1, V)
         assert r0 == covered
         covered = r1
-        assert (r1 - r0 + 255) // 256 <= p["max_tiles"]
+        nu = u1 - u0
+        tiles = 1 if nu <= 2 else (16 * (nu - 2) + 255) // 256 + 1
+        assert tiles <= p["max_tiles"]
         assert r1 > r0
     assert covered == V
     slots = max(p["nCand"], (V + 8191) // 8192)

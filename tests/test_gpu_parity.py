@@ -220,18 +220,27 @@ def test_side_stream_and_workspace_growth(fs, dev):
 
 # ---------------------------------------------------------------- unfused comparator
 
-def test_unfused_f32_equals_fused(fs, dev):
-    B, V, D = 65, 33000, 256
-    g = torch.Generator(device="cpu").manual_seed(5)
+@pytest.mark.parametrize("T", [0.8, 1e-3, 0.3, 50.0, "rows"])
+@pytest.mark.parametrize("B,V,D,scale", [(65, 33000, 256, 0.08), (300, 20011, 64, 0.5),
+                                         (7, 151936, 128, 0.02)])
+def test_unfused_f32_equals_fused(fs, dev, B, V, D, scale, T):
+    """The unfused sampling pass evaluates every element's Gumbel; the fused
+    epilogue screens elements that cannot win.  With f32 logits both must pick
+    the same index with the same score, bit for bit, at any temperature."""
+    g = torch.Generator(device="cpu").manual_seed(B + V)
     H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
-    W = (torch.randn((V, D), generator=g) * 0.08).to(torch.bfloat16).to(dev)
-    fi, fsc, fl = fs.fs_sample_ex(H, W, temperature=0.8, seed=8, offset=1,
-                                  flags=fs.FS_FLAG_STORE_LOGITS)
-    ui, usc, Y = fs.fs_sample_unfused(H, W, temperature=0.8, seed=8, offset=1,
-                                      y_dtype=fs.FS_DTYPE_F32)
-    torch.cuda.synchronize()
-    assert torch.equal(Y, fl)
-    assert torch.equal(fi, ui) and torch.equal(fsc, usc)
+    W = (torch.randn((V, D), generator=g) * scale).to(torch.bfloat16).to(dev)
+    if T == "rows":
+        T = (torch.rand(B, generator=g) * 3.0 + 1e-3).to(dev)
+    for off in (1, 2):
+        fi, fsc, fl = fs.fs_sample_ex(H, W, temperature=T, seed=8, offset=off,
+                                      flags=fs.FS_FLAG_STORE_LOGITS)
+        ui, usc, Y = fs.fs_sample_unfused(H, W, temperature=T, seed=8, offset=off,
+                                          y_dtype=fs.FS_DTYPE_F32)
+        torch.cuda.synchronize()
+        assert torch.equal(Y, fl)
+        assert torch.equal(fi, ui)
+        assert torch.equal(fsc, usc)
 
 
 def test_unfused_bf16_logits(fs, dev):
