@@ -57,11 +57,17 @@ bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *p) {
     p->P = static_cast<int>(P);
     p->G = static_cast<int>(P * nM);
     p->nCand = static_cast<int>(2 * P);
-    // tiles of the largest partition: 256-row tiles, then a final 2-unit tile
+    // Small batches end each partition with a short tile: its epilogue is the
+    // one that cannot overlap an MMA, and re-streaming the few H rows for one
+    // more tile is cheap.  Tiles of the largest partition:
+    p->splitLast = B <= 16;
     const int64_t max_units = (U + P - 1) / P;
-    p->maxTiles = max_units <= 2
-                      ? 1
-                      : static_cast<int>(((max_units - 2) * kUnitRows + kBN - 1) / kBN + 1);
+    if (p->splitLast)
+        p->maxTiles = max_units <= 2
+                          ? 1
+                          : static_cast<int>(((max_units - 2) * kUnitRows + kBN - 1) / kBN + 1);
+    else
+        p->maxTiles = static_cast<int>((max_units * kUnitRows + kBN - 1) / kBN);
     p->nChunks = static_cast<int>((V + kLogitsChunk - 1) / kLogitsChunk);
     const int64_t slots = p->nCand > p->nChunks ? p->nCand : p->nChunks;
     const int64_t region = ((slots * B * 4) + 255) / 256 * 256;
@@ -241,6 +247,7 @@ static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &
     a.y_vec_ok = dst && (reinterpret_cast<uintptr_t>(dst) % 16 == 0) &&
                  (f32 ? (p.V % 4 == 0) : (p.V % 8 == 0));
     a.h_box_rows = h_box_rows;
+    a.split_last = p.splitLast ? 1 : 0;
     a.timeout_ns = wait_timeout_ns();
     cudaError_t e = launch_stage1(mode, tmH, tmW64, tmW16, a, p.G, stream);
     if (e != cudaSuccess) return cuda_fail(e, "Stage 1 launch");

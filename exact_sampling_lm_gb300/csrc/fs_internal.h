@@ -48,6 +48,7 @@ struct Plan {
     int64_t U;     // vocabulary units of 16 rows
     int maxTiles;  // max vocabulary tiles per CTA
     int nChunks;   // blocks per row of the materialised-logits sampler
+    bool splitLast;  // partitions end with a short tile (small batches)
     size_t wsBytes;
 };
 
@@ -67,6 +68,7 @@ struct Stage1Args {
     void *out_y;        // [B][V] bf16/f32 (GEMM modes)
     int y_vec_ok;       // row starts of Y / out_logits are 16-byte aligned
     int h_box_rows;     // rows of the H tensor-map box (8..128; rows above are not loaded)
+    int split_last;     // end each partition with a short (<= 32-row) tile
     uint64_t timeout_ns;
 };
 

@@ -52,18 +52,28 @@ constexpr uint32_t kStatusTimeout = 1u;
 
 __device__ __forceinline__ int round_up16(int x) { return (x + 15) & ~15; }
 
-// Rows [r0, r1) of a partition of nu 16-row units: 256-row tiles over the
-// first nu - 2 units, then one final tile over the last two units (fewer if
-// the partition is that small).  Tile starts are multiples of 16 rows.
+// Rows [r0, r1) of a partition of nu 16-row units.  With split_last (small
+// batches, where re-streaming H for one more tile is cheap): 256-row tiles over
+// the first nu - 2 units, then one final tile over the last two units (fewer
+// if the partition is that small), so the epilogue that cannot overlap an MMA
+// is short.  Otherwise plain 256-row tiles with the remainder last.  Tile
+// starts are multiples of 16 rows.
 struct PartGeom {
     int r0, r1, nu, nmain, ntiles;
 };
 
-__device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V) {
+__device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V, bool split_last) {
     PartGeom g;
     g.r0 = static_cast<int>(u0 * kUnitRows);
     g.r1 = static_cast<int>(min(u1 * kUnitRows, static_cast<int64_t>(V)));
     g.nu = static_cast<int>(u1 - u0);
+    if (!split_last) {
+        // plain 256-row tiles, the remainder last
+        g.nmain = (g.r1 - g.r0 + kBN - 1) / kBN;
+        g.ntiles = g.nmain;
+        g.nu = -1;
+        return g;
+    }
     if (g.nu <= 2) {
         g.nmain = 0;
         g.ntiles = (g.r1 > g.r0) ? 1 : 0;
@@ -75,6 +85,11 @@ __device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V) {
 }
 
 __device__ __forceinline__ void tile_geom(const PartGeom &g, int t, int &v0, int &tn) {
+    if (g.nu < 0) {
+        v0 = g.r0 + kBN * t;
+        tn = min(kBN, g.r1 - v0);
+        return;
+    }
     if (g.nu <= 2) {
         v0 = g.r0;
         tn = g.r1 - g.r0;
@@ -136,11 +151,17 @@ __device__ __forceinline__ void store_bf16_chunk(__nv_bfloat16 *dst, int n,
 
 }  // namespace
 
-template <int MODE>
+// CS = CTAs per cluster (1 or 2).  With CS = 2 the two CTAs of a cluster
+// work on consecutive batch tiles of the same vocabulary partition: each one
+// loads every other W box of a stage and multicasts it to both, so W crosses
+// L2 -> SM once per pair, and each stage is refilled only after both CTAs'
+// MMAs have released it (their commits arrive on both CTAs' empty barriers).
+template <int MODE, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW64,
                   const __grid_constant__ CUtensorMap tmW16, const Stage1Args a) {
     constexpr bool kSample = (MODE == kModeSample || MODE == kModeSampleStore);
+    constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CS) - 1u);
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -161,15 +182,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m = blockIdx.x % a.nM;
     const int part = blockIdx.x / a.nM;
     const PartGeom geom = part_geom(static_cast<int64_t>(part) * a.U / a.P,
-                                    static_cast<int64_t>(part + 1) * a.U / a.P, a.V);
+                                    static_cast<int64_t>(part + 1) * a.U / a.P, a.V,
+                                    a.split_last != 0);
+    const uint32_t crank = (CS > 1) ? cluster_ctarank() : 0u;
     const int ntiles = geom.ntiles;
     const int nk = (a.D + kBK - 1) / kBK;
-    const int kb_first = static_cast<int>(blockIdx.x % static_cast<unsigned>(nk));
+    // The CTAs of a cluster exchange W k-blocks, so they must walk the same
+    // k sequence: rotate by cluster, not by CTA.
+    const int kb_first = static_cast<int>((blockIdx.x / CS) % static_cast<unsigned>(nk));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
+            mbar_init(&empty_bar[s], CS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull_bar[i], 1);
@@ -186,6 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // Both CTAs' barriers must be initialised before either multicasts.
+    if (CS > 1) cluster_sync();
     const uint32_t tmem_base = *tmem_slot;
     // Stage 2 (launched with programmatic serialization) may be scheduled now;
     // it waits for this grid's completion before reading the candidates.
@@ -223,12 +250,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *dB = sB + stage * kBBytes;
                     const int kx = kb * kBK;
                     tma_load_2d(dA, &tmH, &full_bar[stage], kx, m * kBM, pol_h);
-                    for (int i = 0; i < n64; ++i)
-                        tma_load_2d(dB + i * 64 * (kBK * 2), &tmW64, &full_bar[stage], kx,
-                                    v0 + i * 64, pol_w);
-                    for (int i = 0; i < n16; ++i)
-                        tma_load_2d(dB + (n64 * 64 + i * 16) * (kBK * 2), &tmW16, &full_bar[stage],
-                                    kx, v0 + n64 * 64 + i * 16, pol_w);
+                    if (CS == 1) {
+                        for (int i = 0; i < n64; ++i)
+                            tma_load_2d(dB + i * 64 * (kBK * 2), &tmW64, &full_bar[stage], kx,
+                                        v0 + i * 64, pol_w);
+                        for (int i = 0; i < n16; ++i)
+                            tma_load_2d(dB + (n64 * 64 + i * 16) * (kBK * 2), &tmW16,
+                                        &full_bar[stage], kx, v0 + n64 * 64 + i * 16, pol_w);
+                    } else {
+                        // box i of the tile is loaded by cluster rank i % CS
+                        for (int i = static_cast<int>(crank); i < n64 + n16; i += CS) {
+                            if (i < n64)
+                                tma_load_2d_multicast(dB + i * 64 * (kBK * 2), &tmW64,
+                                                      &full_bar[stage], kx, v0 + i * 64,
+                                                      kClusterMask, pol_w);
+                            else
+                                tma_load_2d_multicast(
+                                    dB + (n64 * 64 + (i - n64) * 16) * (kBK * 2), &tmW16,
+                                    &full_bar[stage], kx, v0 + n64 * 64 + (i - n64) * 16,
+                                    kClusterMask, pol_w);
+                        }
+                    }
                     issued_mask |= 1u << stage;
                     last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
@@ -278,7 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      sw128_kmajor_desc(b_addr + ks * kUmmaK * 2), idesc,
                                      (j | ks) != 0 ? 1u : 0u);
                     }
-                    umma_commit(&empty_bar[stage]);
+                    if (CS > 1)
+                        umma_commit_multicast(&empty_bar[stage], kClusterMask);
+                    else
+                        umma_commit(&empty_bar[stage]);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -411,13 +456,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // No CTA leaves while its peer may still multicast into it or arrive on
+    // its barriers.
+    if (CS > 1) cluster_sync();
     if (warp == kWarpMma) {
         __syncwarp();
         tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
-template <int MODE>
+template <int MODE, int CS>
 static cudaError_t launch_mode(const CUtensorMap &tmH, const CUtensorMap &tmW64,
                                const CUtensorMap &tmW16, const Stage1Args &a, int grid,
                                cudaStream_t stream) {
@@ -426,24 +474,87 @@ static cudaError_t launch_mode(const CUtensorMap &tmH, const CUtensorMap &tmW64,
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 32 && !(configured_mask & (1 << dev))) {
-        e = cudaFuncSetAttribute(stage1_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
+        e = cudaFuncSetAttribute(stage1_kernel<MODE, CS>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
+        if (CS > 1) {
+            e = cudaFuncSetAttribute(stage1_kernel<MODE, CS>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+            if (e != cudaSuccess) return e;
+        }
         configured_mask |= 1 << dev;
     }
-    stage1_kernel<MODE><<<grid, kThreads, kSmemBytes, stream>>>(tmH, tmW64, tmW16, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, stage1_kernel<MODE, CS>, tmH, tmW64, tmW16, a);
+}
+
+// How many 2-CTA clusters of Stage 1 the current device can hold at once
+// (cached per device; 0 if the query fails).
+static int max_pair_clusters() {
+    static int cached[64];
+    static bool known[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!known[dev]) {
+        int n = 0;
+        if (cudaFuncSetAttribute(stage1_kernel<kModeSample, 2>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = kSmemBytes;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, stage1_kernel<kModeSample, 2>, &cfg) !=
+                cudaSuccess)
+                n = 0;
+        }
+        cudaGetLastError();  // a failed query leaves no sticky error
+        cached[dev] = n;
+        known[dev] = true;
+    }
+    return cached[dev];
 }
 
 cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const CUtensorMap &tmW64,
                           const CUtensorMap &tmW16, const Stage1Args &a, int grid,
                           cudaStream_t stream) {
+    // Pairs only when batch tiles come in pairs and every pair fits at once.
+    const bool pair = (a.nM % 2 == 0) && (2 * max_pair_clusters() >= grid);
+    if (pair) {
+        switch (mode) {
+            case kModeSample: return launch_mode<kModeSample, 2>(tmH, tmW64, tmW16, a, grid, stream);
+            case kModeSampleStore:
+                return launch_mode<kModeSampleStore, 2>(tmH, tmW64, tmW16, a, grid, stream);
+            case kModeGemmBf16:
+                return launch_mode<kModeGemmBf16, 2>(tmH, tmW64, tmW16, a, grid, stream);
+            case kModeGemmF32: return launch_mode<kModeGemmF32, 2>(tmH, tmW64, tmW16, a, grid, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (mode) {
-        case kModeSample: return launch_mode<kModeSample>(tmH, tmW64, tmW16, a, grid, stream);
+        case kModeSample: return launch_mode<kModeSample, 1>(tmH, tmW64, tmW16, a, grid, stream);
         case kModeSampleStore:
-            return launch_mode<kModeSampleStore>(tmH, tmW64, tmW16, a, grid, stream);
-        case kModeGemmBf16: return launch_mode<kModeGemmBf16>(tmH, tmW64, tmW16, a, grid, stream);
-        case kModeGemmF32: return launch_mode<kModeGemmF32>(tmH, tmW64, tmW16, a, grid, stream);
+            return launch_mode<kModeSampleStore, 1>(tmH, tmW64, tmW16, a, grid, stream);
+        case kModeGemmBf16: return launch_mode<kModeGemmBf16, 1>(tmH, tmW64, tmW16, a, grid, stream);
+        case kModeGemmF32: return launch_mode<kModeGemmF32, 1>(tmH, tmW64, tmW16, a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

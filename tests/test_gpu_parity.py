@@ -222,7 +222,7 @@ def test_side_stream_and_workspace_growth(fs, dev):
 
 @pytest.mark.parametrize("T", [0.8, 1e-3, 0.3, 50.0, "rows"])
 @pytest.mark.parametrize("B,V,D,scale", [(65, 33000, 256, 0.08), (300, 20011, 64, 0.5),
-                                         (7, 151936, 128, 0.02)])
+                                         (7, 151936, 128, 0.02), (256, 30011, 192, 0.1)])
 def test_unfused_f32_equals_fused(fs, dev, B, V, D, scale, T):
     """The unfused sampling pass evaluates every element's Gumbel; the fused
     epilogue screens elements that cannot win.  With f32 logits both must pick
