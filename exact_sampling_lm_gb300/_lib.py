@@ -59,6 +59,7 @@ SIGNATURES = {
     "fs_get_device_status": ([_vp, ctypes.POINTER(_u32)], _int),
     "fs_plan_info": ([_i64, _i64, _i64, _int, ctypes.POINTER(_i64)], _int),
     "fs_release_workspaces": ([], _int),
+    "fs_sample_noalloc": ([_vp, _vp, _i64, _i64, _i64, _f32, _vp, _u64, _u64, _vp, _vp, _vp], _int),
     "fs_last_error_string": ([], ctypes.c_char_p),
     "fs_version": ([], ctypes.c_char_p),
 }
@@ -278,6 +279,21 @@ def fs_get_device_status(stream=None) -> int:
     if st not in (FS_OK, FS_ERR_TIMEOUT):
         _check(st)
     return int(w.value)
+
+
+def fs_sample_noalloc(H, W, temperature=1.0, seed=0, offset=0, out_idx=None, out_score=None,
+                      want_score=True, stream=None):
+    """fs_sample without any device allocation by the library (static scratch).
+    Output tensors are allocated here by torch unless the caller passes them."""
+    _check_matrix("H", H, torch.bfloat16)
+    _check_matrix("W", W, torch.bfloat16)
+    B, D = H.shape
+    V = W.shape[0]
+    T, Tv = _temps(temperature, H.device)
+    out_idx, out_score = _outs(B, H.device, out_idx, out_score, want_score)
+    _check(lib().fs_sample_noalloc(_ptr(H), _ptr(W), B, V, D, T, _ptr(Tv), seed, offset,
+                                   _ptr(out_idx), _ptr(out_score), _stream(stream)))
+    return out_idx, out_score
 
 
 def fs_release_workspaces():

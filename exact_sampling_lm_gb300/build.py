@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libfs_sample.so")
 
-SOURCES = ["fs_api.cu", "fs_stage1.cu", "fs_small.cu"]
+SOURCES = ["fs_api.cu", "fs_stage1.cu", "fs_small.cu", "fs_noalloc.cu"]
 HEADERS = ["fs_internal.h", "fs_noise.cuh", "fs_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

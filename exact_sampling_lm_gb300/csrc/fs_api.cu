@@ -32,6 +32,18 @@ static fs_status fail(fs_status st, const char *fmt, ...) {
     return st;
 }
 
+// Records the thread-local error text for entry points defined in other
+// translation units.
+fs_status set_error(fs_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
 static fs_status cuda_fail(cudaError_t e, const char *what) {
     return fail(FS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }

@@ -186,6 +186,30 @@ fs_status fs_get_device_status(void *stream, uint32_t *out_word);
  * ------------------------------------------------------------------------- */
 fs_status fs_plan_info(int64_t B, int64_t V, int64_t D, int num_sms, int64_t out[6]);
 
+/* ---------------------------------------------------------------------------
+ * fs_sample_noalloc -- fs_sample that allocates no device memory.  The paper
+ * has no counterpart: this is a library convenience.  It is for callers that
+ * cannot allocate: applications that reserve all device memory up front and
+ * forbid allocation afterwards (an inference server's own memory pool, a
+ * plug-in whose host owns the allocator), and decode loops that cannot afford
+ * cudaMalloc's possible device synchronisation.
+ * Arguments, results and errors are those of fs_sample.  The candidate
+ * scratch is a static array of FS_NOALLOC_SCRATCH_BYTES inside the library's
+ * device memory (held on every GPU that loads the library until the process
+ * exits); a call whose candidates need more (fs_workspace_size(B, V, D) >
+ * FS_NOALLOC_SCRATCH_BYTES) returns FS_ERR_UNSUPPORTED and launches nothing.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress), so make that first call before any stream capture.
+ * All calls share the array: calls whose kernels overlap on the GPU (other
+ * streams, other host threads) race on it and must be serialised by the
+ * caller.  Nothing in it needs clearing between calls.
+ * ------------------------------------------------------------------------- */
+#define FS_NOALLOC_SCRATCH_BYTES (1 << 20)
+fs_status fs_sample_noalloc(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                            float temperature, const float *temperatures, uint64_t seed,
+                            uint64_t offset, int64_t *out_idx, float *out_score,
+                            void *stream);
+
 /* Frees every workspace cached by fs_sample (all devices and streams).  The
  * caller must make sure no fs_sample call is still running on the GPU. */
 fs_status fs_release_workspaces(void);
