@@ -68,18 +68,14 @@ bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *p) {
     p->U = U;
     p->P = static_cast<int>(P);
     p->G = static_cast<int>(P * nM);
-    p->nCand = static_cast<int>(2 * P);
-    // Small batches end each partition with a short tile: its epilogue is the
-    // one that cannot overlap an MMA, and re-streaming the few H rows for one
-    // more tile is cheap.  Tiles of the largest partition:
-    p->splitLast = B <= 16;
+    p->nCand = static_cast<int>(P);
+    // Tiles of the largest partition: balanced tiles of at most 256 rows, then
+    // a final 128-row tile (a partition of at most 256 rows is one tile).
     const int64_t max_units = (U + P - 1) / P;
-    if (p->splitLast)
-        p->maxTiles = max_units <= 2
-                          ? 1
-                          : static_cast<int>(((max_units - 2) * kUnitRows + kBN - 1) / kBN + 1);
-    else
-        p->maxTiles = static_cast<int>((max_units * kUnitRows + kBN - 1) / kBN);
+    const int64_t main_units = max_units - kFinalTileUnits;
+    p->maxTiles = max_units <= kBN / kUnitRows
+                      ? 1
+                      : static_cast<int>((main_units + kBN / kUnitRows - 1) / (kBN / kUnitRows) + 1);
     p->nChunks = static_cast<int>((V + kLogitsChunk - 1) / kLogitsChunk);
     const int64_t slots = p->nCand > p->nChunks ? p->nCand : p->nChunks;
     const int64_t region = ((slots * B * 4) + 255) / 256 * 256;
@@ -259,7 +255,6 @@ static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &
     a.y_vec_ok = dst && (reinterpret_cast<uintptr_t>(dst) % 16 == 0) &&
                  (f32 ? (p.V % 4 == 0) : (p.V % 8 == 0));
     a.h_box_rows = h_box_rows;
-    a.split_last = p.splitLast ? 1 : 0;
     a.timeout_ns = wait_timeout_ns();
     cudaError_t e = launch_stage1(mode, tmH, tmW64, tmW16, a, p.G, stream);
     if (e != cudaSuccess) return cuda_fail(e, "Stage 1 launch");

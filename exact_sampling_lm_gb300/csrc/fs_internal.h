@@ -20,12 +20,15 @@ constexpr int kStages = 4;
 constexpr int kUmmaK = 16;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KiB: H tile
 constexpr int kBBytes = kBN * kBK * 2;  // 32 KiB: W tile
-constexpr int kNumEpiWarps = 8;         // 2 per TMEM lane quarter
-constexpr int kWarpTma = 8;
-constexpr int kWarpMma = 9;
-constexpr int kThreads = 320;
+constexpr int kColParts = 4;                      // epilogue warps per TMEM lane quarter
+constexpr int kNumEpiWarps = 4 * kColParts;       // 16
+constexpr int kWarpTma = kNumEpiWarps;            // warp 16
+constexpr int kWarpMma = kNumEpiWarps + 1;        // warp 17
+constexpr int kThreads = (kNumEpiWarps + 2) * 32; // 576
 constexpr int kTmemCols = 512;  // two 256-column accumulators
-constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 1024 + 256;
+constexpr int kCombineBytes = kColParts * kBM * 8;  // per-row bests of the column parts
+constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 1024 + 256 + kCombineBytes;
+constexpr int kFinalTileUnits = 8;  // last tile of a partition: 128 rows
 constexpr int kUnitRows = 16;  // vocabulary partitions are multiples of 16 rows
 
 // ---- materialised-logits sampler ------------------------------------------
@@ -44,11 +47,10 @@ struct Plan {
     int nM;        // batch tiles of 128 rows
     int P;         // vocabulary partitions (one per CTA column)
     int G;         // CTAs launched = P * nM
-    int nCand;     // candidate slots per row (2 per partition: two column halves)
+    int nCand;     // candidate slots per row (one per partition)
     int64_t U;     // vocabulary units of 16 rows
     int maxTiles;  // max vocabulary tiles per CTA
     int nChunks;   // blocks per row of the materialised-logits sampler
-    bool splitLast;  // partitions end with a short tile (small batches)
     size_t wsBytes;
 };
 
@@ -68,7 +70,6 @@ struct Stage1Args {
     void *out_y;        // [B][V] bf16/f32 (GEMM modes)
     int y_vec_ok;       // row starts of Y / out_logits are 16-byte aligned
     int h_box_rows;     // rows of the H tensor-map box (8..128; rows above are not loaded)
-    int split_last;     // end each partition with a short (<= 32-row) tile
     uint64_t timeout_ns;
 };
 

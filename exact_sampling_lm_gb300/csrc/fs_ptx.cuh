@@ -68,6 +68,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// As mbar_wait_bounded, for waits that are long by design (epilogue warps
+// waiting for a whole tile's MMA): after a short spin it sleeps between polls
+// so that idle warps leave the issue slots (and power) to the busy ones.
+__device__ __forceinline__ bool mbar_wait_bounded_backoff(uint64_t *bar, uint32_t parity,
+                                                          uint64_t limit_ns,
+                                                          volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (it > 8) __nanosleep(200);
+        if ((it & 15u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -52,57 +52,59 @@ constexpr uint32_t kStatusTimeout = 1u;
 
 __device__ __forceinline__ int round_up16(int x) { return (x + 15) & ~15; }
 
-// Rows [r0, r1) of a partition of nu 16-row units.  With split_last (small
-// batches, where re-streaming H for one more tile is cheap): 256-row tiles over
-// the first nu - 2 units, then one final tile over the last two units (fewer
-// if the partition is that small), so the epilogue that cannot overlap an MMA
-// is short.  Otherwise plain 256-row tiles with the remainder last.  Tile
-// starts are multiples of 16 rows.
+// Rows [r0, r1) of a partition of nu 16-row units.  A partition of at most
+// 256 rows is one tile.  A larger one ends with a 128-row tile -- its
+// epilogue is the one that cannot overlap an MMA, so it should be short --
+// and splits the rest evenly into tiles of at most 256 rows, so that every
+// pipeline stage still carries enough W bytes to keep HBM busy.  Tile starts
+// are multiples of 16 rows.
 struct PartGeom {
     int r0, r1, nu, nmain, ntiles;
 };
 
-__device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V, bool split_last) {
+__device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V) {
+    constexpr int kTileUnits = kBN / kUnitRows;
     PartGeom g;
     g.r0 = static_cast<int>(u0 * kUnitRows);
     g.r1 = static_cast<int>(min(u1 * kUnitRows, static_cast<int64_t>(V)));
     g.nu = static_cast<int>(u1 - u0);
-    if (!split_last) {
-        // plain 256-row tiles, the remainder last
-        g.nmain = (g.r1 - g.r0 + kBN - 1) / kBN;
-        g.ntiles = g.nmain;
-        g.nu = -1;
-        return g;
-    }
-    if (g.nu <= 2) {
+    if (g.nu <= kTileUnits) {
         g.nmain = 0;
         g.ntiles = (g.r1 > g.r0) ? 1 : 0;
     } else {
-        g.nmain = (kUnitRows * (g.nu - 2) + kBN - 1) / kBN;
+        g.nmain = (g.nu - kFinalTileUnits + kTileUnits - 1) / kTileUnits;
         g.ntiles = g.nmain + 1;
     }
     return g;
 }
 
 __device__ __forceinline__ void tile_geom(const PartGeom &g, int t, int &v0, int &tn) {
-    if (g.nu < 0) {
-        v0 = g.r0 + kBN * t;
-        tn = min(kBN, g.r1 - v0);
-        return;
-    }
-    if (g.nu <= 2) {
+    if (g.nmain == 0) {
         v0 = g.r0;
         tn = g.r1 - g.r0;
         return;
     }
-    const int main_rows = kUnitRows * (g.nu - 2);
+    const int main_units = g.nu - kFinalTileUnits;
     if (t < g.nmain) {
-        v0 = g.r0 + kBN * t;
-        tn = min(kBN, main_rows - kBN * t);
+        const int s = main_units * t / g.nmain;
+        const int e = main_units * (t + 1) / g.nmain;
+        v0 = g.r0 + kUnitRows * s;
+        tn = kUnitRows * (e - s);
     } else {
-        v0 = g.r0 + main_rows;
+        v0 = g.r0 + kUnitRows * main_units;
         tn = g.r1 - v0;
     }
+}
+
+// First column of column part j (of kColParts) of a tile of width tn: parts
+// start on 16-column boundaries; part kColParts ends at tn.
+__device__ __forceinline__ int col_part_start(int j, int tn) {
+    if (j >= kColParts) return tn;
+    return min(tn, round_up16((j * tn + kColParts - 1) / kColParts));
+}
+
+__device__ __forceinline__ void epilogue_barrier() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kNumEpiWarps * 32) : "memory");
 }
 
 __device__ __forceinline__ void raise_timeout(volatile int *abort_flag) {
@@ -176,14 +178,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *done_bar = tempty_bar + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *comb_s = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 256);
+    int *comb_i = reinterpret_cast<int *>(comb_s + kColParts * kBM);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int m = blockIdx.x % a.nM;
     const int part = blockIdx.x / a.nM;
     const PartGeom geom = part_geom(static_cast<int64_t>(part) * a.U / a.P,
-                                    static_cast<int64_t>(part + 1) * a.U / a.P, a.V,
-                                    a.split_last != 0);
+                                    static_cast<int64_t>(part + 1) * a.U / a.P, a.V);
     const uint32_t crank = (CS > 1) ? cluster_ctarank() : 0u;
     const int ntiles = geom.ntiles;
     const int nk = (a.D + kBK - 1) / kBK;
@@ -196,9 +199,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], CS);
         }
+        // Only epilogue warps whose TMEM lane quarter holds live batch rows
+        // take part in the tile loop and release the accumulators.
+        const int live_rows = min(kBM, a.B - m * kBM);
+        const int live_quarters = (live_rows + 31) / 32;
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull_bar[i], 1);
-            mbar_init(&tempty_bar[i], kNumEpiWarps);
+            mbar_init(&tempty_bar[i], kColParts * live_quarters);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -338,8 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------ epilogue warps
-        const int q = warp & 3;  // TMEM lane quarter
-        const int h = warp >> 2; // column half of the tile
+        const int q = warp & 3;   // TMEM lane quarter (the warp's rank in its warpgroup)
+        const int j = warp >> 2;  // column part of the tile
         const int row = q * 32 + lane;
         const int b = m * kBM + row;
         const bool warp_has_rows = (m * kBM + q * 32) < a.B;
@@ -356,21 +363,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         float best = -INFINITY;
         int bidx = -1;
         bool ok = true;
-        for (int t = 0; t < ntiles; ++t) {
+        // Warps without live rows skip the tile loop (they are not counted by
+        // the accumulator-release barrier) and wait at the combine barrier.
+        for (int t = 0; t < (warp_has_rows ? ntiles : 0); ++t) {
             const int acc = t & 1;
             const uint32_t aphase = static_cast<uint32_t>(t >> 1) & 1u;
-            if (!mbar_wait_bounded(&tfull_bar[acc], aphase, a.timeout_ns, abort_flag)) {
+            if (!mbar_wait_bounded_backoff(&tfull_bar[acc], aphase, a.timeout_ns, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
             int v0, tn;
             tile_geom(geom, t, v0, tn);
-            // Columns split between the two halves in 16-column steps.
-            const int cs = min(tn, round_up16((tn + 1) >> 1));
-            const int c_lo = h ? cs : 0;
-            const int c_hi = h ? tn : cs;
-            if (warp_has_rows) {
+            const int c_lo = col_part_start(j, tn);
+            const int c_hi = col_part_start(j + 1, tn);
+            {
                 for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
                     uint32_t r[16];
                     tmem_ld16_wait(tmem_base + static_cast<uint32_t>(acc * kBN + c0) +
@@ -446,10 +453,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&tempty_bar[acc]);
         }
         if (!ok) raise_timeout(abort_flag);
-        if (kSample && row_ok) {
-            const size_t slot = static_cast<size_t>(part) * 2 + h;
-            a.cand_score[slot * a.B + b] = best;
-            a.cand_idx[slot * a.B + b] = bidx;
+        if (kSample) {
+            // Combine the column parts' bests of each row (tie: lower index),
+            // then one candidate per (row, partition).
+            comb_s[j * kBM + row] = best;
+            comb_i[j * kBM + row] = bidx;
+            epilogue_barrier();
+            if (j == 0 && row_ok) {
+#pragma unroll
+                for (int jj = 1; jj < kColParts; ++jj) {
+                    const float s = comb_s[jj * kBM + row];
+                    const int i = comb_i[jj * kBM + row];
+                    if (s > best ||
+                        (s == best && static_cast<uint32_t>(i) < static_cast<uint32_t>(bidx))) {
+                        best = s;
+                        bidx = i;
+                    }
+                }
+                a.cand_score[static_cast<size_t>(part) * a.B + b] = best;
+                a.cand_idx[static_cast<size_t>(part) * a.B + b] = bidx;
+            }
         }
     }
 

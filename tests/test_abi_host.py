@@ -62,13 +62,13 @@ def test_version_and_error_string():
                                        (300, 50257, 72, 148), (3, 5, 8, 152)])
 def test_plan_covers_the_vocabulary(B, V, D, sms):
     """Partitions are disjoint, cover [0, V) in 16-row units, and every CTA
-    gets at most max_tiles tiles (256-row tiles, then a final tile of the last
-    two units); one CTA per SM at most."""
+    gets at most max_tiles tiles (balanced tiles of <= 256 rows, then a final
+    128-row tile); one CTA per SM at most."""
     p = fs.fs_plan_info(B, V, D, sms)
     nM = (B + 127) // 128
     assert p["nM"] == nM
     assert p["G"] == p["P"] * nM <= max(sms, nM)
-    assert p["nCand"] == 2 * p["P"]
+    assert p["nCand"] == p["P"]
     U = (V + 15) // 16
     covered = 0
     for part in range(p["P"]):
@@ -78,10 +78,7 @@ def test_plan_covers_the_vocabulary(B, V, D, sms):
         assert r0 == covered
         covered = r1
         nu = u1 - u0
-        if B <= 16:  # short final tile
-            tiles = 1 if nu <= 2 else (16 * (nu - 2) + 255) // 256 + 1
-        else:
-            tiles = (r1 - r0 + 255) // 256
+        tiles = 1 if nu <= 16 else (nu - 8 + 15) // 16 + 1
         assert tiles <= p["max_tiles"]
         assert r1 > r0
     assert covered == V
