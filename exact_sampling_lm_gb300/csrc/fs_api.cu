@@ -70,12 +70,16 @@ bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *p) {
     p->G = static_cast<int>(P * nM);
     p->nCand = static_cast<int>(P);
     // Tiles of the largest partition: balanced tiles of at most 256 rows, then
-    // a final 128-row tile (a partition of at most 256 rows is one tile).
+    // a final 128-row tile (a partition of at most 256 rows is one tile); CTAs
+    // paired in clusters (an even nM) use plain 256-row tiles.
     const int64_t max_units = (U + P - 1) / P;
     const int64_t main_units = max_units - kFinalTileUnits;
-    p->maxTiles = max_units <= kBN / kUnitRows
-                      ? 1
-                      : static_cast<int>((main_units + kBN / kUnitRows - 1) / (kBN / kUnitRows) + 1);
+    if (nM % 2 == 0)
+        p->maxTiles = static_cast<int>((max_units * kUnitRows + kBN - 1) / kBN);
+    else
+        p->maxTiles = max_units <= kBN / kUnitRows
+                          ? 1
+                          : static_cast<int>((main_units + kBN / kUnitRows - 1) / (kBN / kUnitRows) + 1);
     p->nChunks = static_cast<int>((V + kLogitsChunk - 1) / kLogitsChunk);
     const int64_t slots = p->nCand > p->nChunks ? p->nCand : p->nChunks;
     const int64_t region = ((slots * B * 4) + 255) / 256 * 256;

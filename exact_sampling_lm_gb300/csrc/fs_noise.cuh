@@ -135,4 +135,14 @@ __device__ __forceinline__ float screen_threshold(float d) {
     return thr * (1.0f - 0x1p-12f);
 }
 
+// Integer form of the screen for a group of elements: the largest k with
+// k * 2^-24 <= screen_threshold(d), so that an element with 24-bit numerator
+// kx = (x >> 8) | 1 passes the screen iff kx > screen_kbound(d).  For NaN d
+// it returns 0 (every element takes the exact path).  A group of elements may
+// share one bound computed at the group's smallest d (largest transformed
+// logit): the threshold rises with d, so that bound is the most permissive.
+__device__ __forceinline__ uint32_t screen_kbound(float d) {
+    return __float2uint_rd(screen_threshold(d) * 0x1p24f);
+}
+
 }  // namespace fs

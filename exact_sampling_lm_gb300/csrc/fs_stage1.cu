@@ -56,18 +56,27 @@ __device__ __forceinline__ int round_up16(int x) { return (x + 15) & ~15; }
 // 256 rows is one tile.  A larger one ends with a 128-row tile -- its
 // epilogue is the one that cannot overlap an MMA, so it should be short --
 // and splits the rest evenly into tiles of at most 256 rows, so that every
-// pipeline stage still carries enough W bytes to keep HBM busy.  Tile starts
-// are multiples of 16 rows.
+// pipeline stage still carries enough W bytes to keep HBM busy.  CTAs that
+// share W tiles in a cluster (full_tiles) use plain 256-row tiles with the
+// remainder last instead: each of them receives the whole tile, so they need
+// the largest stages to keep enough bytes in flight.  Tile starts are
+// multiples of 16 rows.
 struct PartGeom {
     int r0, r1, nu, nmain, ntiles;
 };
 
-__device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V) {
+__device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V, bool full_tiles) {
     constexpr int kTileUnits = kBN / kUnitRows;
     PartGeom g;
     g.r0 = static_cast<int>(u0 * kUnitRows);
     g.r1 = static_cast<int>(min(u1 * kUnitRows, static_cast<int64_t>(V)));
     g.nu = static_cast<int>(u1 - u0);
+    if (full_tiles) {
+        // 256-row tiles, the remainder last
+        g.nmain = -1;
+        g.ntiles = (g.r1 - g.r0 + kBN - 1) / kBN;
+        return g;
+    }
     if (g.nu <= kTileUnits) {
         g.nmain = 0;
         g.ntiles = (g.r1 > g.r0) ? 1 : 0;
@@ -79,6 +88,11 @@ __device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V) {
 }
 
 __device__ __forceinline__ void tile_geom(const PartGeom &g, int t, int &v0, int &tn) {
+    if (g.nmain < 0) {
+        v0 = g.r0 + kBN * t;
+        tn = min(kBN, g.r1 - v0);
+        return;
+    }
     if (g.nmain == 0) {
         v0 = g.r0;
         tn = g.r1 - g.r0;
@@ -186,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m = blockIdx.x % a.nM;
     const int part = blockIdx.x / a.nM;
     const PartGeom geom = part_geom(static_cast<int64_t>(part) * a.U / a.P,
-                                    static_cast<int64_t>(part + 1) * a.U / a.P, a.V);
+                                    static_cast<int64_t>(part + 1) * a.U / a.P, a.V, CS > 1);
     const uint32_t crank = (CS > 1) ? cluster_ctarank() : 0u;
     const int ntiles = geom.ntiles;
     const int nk = (a.D + kBK - 1) / kBK;
@@ -221,9 +235,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Both CTAs' barriers must be initialised before either multicasts.
     if (CS > 1) cluster_sync();
     const uint32_t tmem_base = *tmem_slot;
-    // Stage 2 (launched with programmatic serialization) may be scheduled now;
-    // it waits for this grid's completion before reading the candidates.
-    griddep_launch_dependents();
 
     if (warp == kWarpTma) {
         // ------------------------------------------------ TMA producer
@@ -386,56 +397,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int n_valid = min(16, c_hi - c0);
                     const int vbase = v0 + c0;
                     if (kSample) {
+                        if (MODE == kModeSampleStore && row_ok)
+                            store_f32_chunk(a.out_logits + static_cast<size_t>(b) * a.V + vbase,
+                                            n_valid, r, a.y_vec_ok != 0);
                         if (row_ok && t_ok) {
+                            if (no_noise) {
 #pragma unroll
-                            for (int g8 = 0; g8 < 2; ++g8) {
-                                if (g8 * 8 < n_valid) {
-                                    if (no_noise) {
+                                for (int i = 0; i < 16; ++i) {
+                                    const float s = __fmul_rn(__uint_as_float(r[i]), invT);
+                                    if (i < n_valid && s > best) {
+                                        best = s;
+                                        bidx = vbase + i;
+                                    }
+                                }
+                            } else {
+                                // Both Philox blocks of the chunk first (two
+                                // independent chains for the scheduler).
+                                uint32_t xa[8], xb[8];
+                                noise_words8(prow, static_cast<uint64_t>(vbase) >> 3, xa);
+                                if (n_valid > 8)
+                                    noise_words8(prow, (static_cast<uint64_t>(vbase) >> 3) + 1, xb);
+                                float lt[16];
+                                float lmax_a = -INFINITY, lmax_b = -INFINITY;
 #pragma unroll
-                                        for (int e = 0; e < 8; ++e) {
-                                            const int i = g8 * 8 + e;
-                                            const float s = __fmul_rn(__uint_as_float(r[i]), invT);
-                                            if (i < n_valid && s > best) {
-                                                best = s;
-                                                bidx = vbase + i;
-                                            }
-                                        }
-                                    } else {
-                                        uint32_t x[8];
-                                        noise_words8(prow, static_cast<uint64_t>(vbase + g8 * 8) >> 3, x);
-                                        // Screen the 8 elements against the best
-                                        // known before the group (a lower bound of
-                                        // the running best, so still conservative),
-                                        // then scan the survivors exactly, in order.
-                                        const float best0 = best;
-                                        float lt[8];
-                                        bool pass[8];
+                                for (int i = 0; i < 16; ++i) {
+                                    lt[i] = __fmul_rn(__uint_as_float(r[i]), invT);
+                                    if (i < n_valid) {
+                                        if (i < 8)
+                                            lmax_a = fmaxf(lmax_a, lt[i]);
+                                        else
+                                            lmax_b = fmaxf(lmax_b, lt[i]);
+                                    }
+                                }
+                                // One conservative screen bound per group of 8,
+                                // against the best known before the chunk (a
+                                // lower bound of the running best); survivors
+                                // are scanned exactly, in order.
+                                const float best0 = best;
+                                const uint32_t kb_a = screen_kbound(best0 - lmax_a);
+                                const uint32_t kb_b = screen_kbound(best0 - lmax_b);
+                                bool pass[16];
 #pragma unroll
-                                        for (int e = 0; e < 8; ++e) {
-                                            const int i = g8 * 8 + e;
-                                            lt[e] = __fmul_rn(__uint_as_float(r[i]), invT);
-                                            pass[e] = (i < n_valid) &&
-                                                      (uniform_from_word(x[e]) >
-                                                       screen_threshold(best0 - lt[e]));
-                                        }
+                                for (int i = 0; i < 16; ++i) {
+                                    const uint32_t xi = i < 8 ? xa[i] : xb[i - 8];
+                                    pass[i] = (i < n_valid) &&
+                                              (((xi >> 8) | 1u) > (i < 8 ? kb_a : kb_b));
+                                }
 #pragma unroll
-                                        for (int e = 0; e < 8; ++e) {
-                                            if (pass[e]) {
-                                                const float s =
-                                                    __fadd_rn(lt[e], gumbel_from_word(x[e]));
-                                                if (s > best) {
-                                                    best = s;
-                                                    bidx = vbase + g8 * 8 + e;
-                                                }
-                                            }
+                                for (int i = 0; i < 16; ++i) {
+                                    if (pass[i]) {
+                                        const uint32_t xi = i < 8 ? xa[i] : xb[i - 8];
+                                        const float s = __fadd_rn(lt[i], gumbel_from_word(xi));
+                                        if (s > best) {
+                                            best = s;
+                                            bidx = vbase + i;
                                         }
                                     }
                                 }
                             }
                         }
-                        if (MODE == kModeSampleStore && row_ok)
-                            store_f32_chunk(a.out_logits + static_cast<size_t>(b) * a.V + vbase,
-                                            n_valid, r, a.y_vec_ok != 0);
                     } else if (row_ok) {
                         if (MODE == kModeGemmF32)
                             store_f32_chunk(static_cast<float *>(a.out_y) +
@@ -479,6 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // This CTA's candidates are written: Stage 2 (launched with programmatic
+    // serialization) may now be scheduled; it still waits for the whole grid
+    // before reading.  Triggering only here keeps its blocks off the SMs while
+    // the epilogues run.
+    griddep_launch_dependents();
     // No CTA leaves while its peer may still multicast into it or arrive on
     // its barriers.
     if (CS > 1) cluster_sync();

@@ -275,6 +275,35 @@ void oracle_sample(const uint16_t *H, const uint16_t *W, int64_t B, int64_t V,
     free(s);
 }
 
+/* ---------------------------------------------------------------------------
+ * Log-probability of a sampled token under softmax(l~): l~[idx] - log sum_v
+ * exp(l~[v]), with l~ = fl(l * fl(1/T)) in f32 as in the sampling pass and the
+ * log-sum-exp evaluated in fp64 as (l~[idx] - max) - log sum exp(l~ - max).  This is the
+ * "local log-mass" summary the grouped / tensor-parallel variant returns per
+ * shard, reduced here over the whole vocabulary.  For each row of f32 logits
+ * [B, V]: out[b] = logprob of idx[b] (NaN when idx[b] < 0 or T[b] invalid).
+ * ------------------------------------------------------------------------- */
+void oracle_logprob(const float *logits, int64_t B, int64_t V, const float *T,
+                    const int64_t *idx, double *out) {
+    for (int64_t b = 0; b < B; ++b) {
+        float Tb = T[b];
+        if (!temperature_ok(Tb) || idx[b] < 0 || idx[b] >= V) {
+            out[b] = NAN;
+            continue;
+        }
+        float invT = 1.0f / Tb;
+        const float *l = logits + b * V;
+        double mx = -INFINITY;
+        for (int64_t v = 0; v < V; ++v) {
+            double x = (double)(l[v] * invT);
+            if (x > mx) mx = x;
+        }
+        double sum = 0.0;
+        for (int64_t v = 0; v < V; ++v) sum += exp((double)(l[v] * invT) - mx);
+        out[b] = ((double)(l[idx[b]] * invT) - mx) - log(sum);
+    }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -52,6 +52,8 @@ def _load():
         lib.oracle_sample.argtypes = [vp, vp, i64, i64, i64, vp, vp, u64, u64, u32,
                                       vp, vp, vp, vp, i32]
         lib.oracle_sample.restype = None
+        lib.oracle_logprob.argtypes = [vp, i64, i64, vp, vp, vp]
+        lib.oracle_logprob.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         _lib = lib
@@ -194,6 +196,17 @@ def sample(H_bits, W_bits, T, seed, offset, flags=0, want_logits=False, nthreads
     return idx, best, second, l64
 
 
-__all__ = ["NO_NOISE", "num_threads", "philox4x64_10", "noise_word", "uniform",
+def logprob(l32, T, idx):
+    """log softmax(l~)[idx] per row in fp64, l~ = fl(l * fl(1/T)) (f32 logits [B, V])."""
+    L = _c(l32, np.float32)
+    B, V = L.shape
+    Tv = _temps(T, B)
+    ix = np.ascontiguousarray(idx, dtype=np.int64)
+    out = np.zeros(B, dtype=np.float64)
+    _load().oracle_logprob(_ptr(L), B, V, _ptr(Tv), _ptr(ix), _ptr(out))
+    return out
+
+
+__all__ = ["logprob", "NO_NOISE", "num_threads", "philox4x64_10", "noise_word", "uniform",
            "gumbel_from_word", "gumbel", "uniform_block", "gumbel_block", "noise_block", "logits",
            "sample_from_logits", "sample"]

@@ -241,3 +241,43 @@ def test_row_ids_key_the_noise_like_the_full_batch():
     sub = oracle.sample(H[rows], W, T[rows], 5, 6, row_ids=rows)
     for a, b in zip(full[:3], sub[:3]):
         assert np.array_equal(a[rows], b)
+
+
+# ---------------------------------------------------------------- log-probability
+
+def test_logprob_matches_scipy_log_softmax():
+    """The sampled token's log-probability (the log-mass summary) against
+    scipy's log_softmax of the same f32-transformed logits."""
+    rng = np.random.default_rng(31)
+    B, V = 7, 5000
+    L = (2.5 * rng.standard_normal((B, V))).astype(np.float32)
+    T = rng.uniform(0.3, 2.0, size=B).astype(np.float32)
+    idx = oracle.sample_from_logits(L, T, 3, 4)[0]
+    got = oracle.logprob(L, T, idx)
+    for b in range(B):
+        lt = (L[b] * (np.float32(1.0) / T[b])).astype(np.float64)
+        want = scipy.special.log_softmax(lt)[idx[b]]
+        assert abs(got[b] - want) < 1e-10
+
+
+def test_logprob_closed_forms():
+    V = 1000
+    L = np.zeros((3, V), dtype=np.float32)
+    L[1, 7] = 50.0  # one dominant token
+    L[2, :] = np.float32(-1e30)  # huge negative but equal
+    idx = np.array([5, 7, 999])
+    got = oracle.logprob(L, np.ones(3, dtype=np.float32), idx)
+    assert abs(got[0] - (-np.log(V))) < 1e-12
+    assert abs(got[1] - (-np.log1p((V - 1) * np.exp(-50.0)))) < 1e-12
+    assert abs(got[2] - (-np.log(V))) < 1e-12
+    bad = oracle.logprob(L, np.array([1.0, 0.0, 1.0], dtype=np.float32), np.array([-1, 3, 2]))
+    assert np.isnan(bad[0]) and np.isnan(bad[1]) and not np.isnan(bad[2])
+
+
+def test_logprob_probabilities_sum_to_one():
+    rng = np.random.default_rng(2)
+    V = 300
+    l = (3 * rng.standard_normal(V)).astype(np.float32)
+    L = np.broadcast_to(l, (V, V))
+    lp = oracle.logprob(L, np.full(V, 0.7, dtype=np.float32), np.arange(V))
+    assert abs(np.exp(lp).sum() - 1.0) < 1e-12
