@@ -117,6 +117,22 @@ __device__ __forceinline__ int col_part_start(int j, int tn) {
     return min(tn, round_up16((j * tn + kColParts - 1) / kColParts));
 }
 
+// Element i (0..15) of a register array, by a chain of selects (an indexed
+// load would move the array to local memory).
+__device__ __forceinline__ float pick16(const float (&a)[16], int i) {
+    float r = a[0];
+#pragma unroll
+    for (int k = 1; k < 16; ++k) r = (i == k) ? a[k] : r;
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pick16x(const uint32_t (&a)[8], const uint32_t (&b)[8], int i) {
+    uint32_t r = a[0];
+#pragma unroll
+    for (int k = 1; k < 16; ++k) r = (i == k) ? (k < 8 ? a[k] : b[k - 8]) : r;
+    return r;
+}
+
 __device__ __forceinline__ void epilogue_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(kNumEpiWarps * 32) : "memory");
 }
@@ -436,22 +452,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const float best0 = best;
                                 const uint32_t kb_a = screen_kbound(best0 - lmax_a);
                                 const uint32_t kb_b = screen_kbound(best0 - lmax_b);
-                                bool pass[16];
+                                uint32_t pass = 0;
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) {
                                     const uint32_t xi = i < 8 ? xa[i] : xb[i - 8];
-                                    pass[i] = (i < n_valid) &&
-                                              (((xi >> 8) | 1u) > (i < 8 ? kb_a : kb_b));
+                                    if (i < n_valid && ((xi >> 8) | 1u) > (i < 8 ? kb_a : kb_b))
+                                        pass |= 1u << i;
                                 }
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    if (pass[i]) {
-                                        const uint32_t xi = i < 8 ? xa[i] : xb[i - 8];
-                                        const float s = __fadd_rn(lt[i], gumbel_from_word(xi));
-                                        if (s > best) {
-                                            best = s;
-                                            bidx = vbase + i;
-                                        }
+                                // Exact scores only for the survivors, lowest
+                                // index first (keeps the tie rule).  A loop over
+                                // the set bits costs one iteration per survivor
+                                // instead of a predicated evaluation of every
+                                // element.
+                                while (pass) {
+                                    const int i = __ffs(pass) - 1;
+                                    pass &= pass - 1;
+                                    const float s =
+                                        __fadd_rn(pick16(lt, i), gumbel_from_word(pick16x(xa, xb, i)));
+                                    if (s > best) {
+                                        best = s;
+                                        bidx = vbase + i;
                                     }
                                 }
                             }
