@@ -50,6 +50,8 @@ SIGNATURES = {
     "fs_stage1": ([_vp, _vp, _i64, _i64, _i64, _f32, _vp, _u64, _u64, _u32, _vp, _vp, _sz, _vp],
                   _int),
     "fs_stage2": ([_i64, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _sz, _vp], _int),
+    "fs_sample_logprob": ([_vp, _vp, _i64, _i64, _i64, _f32, _vp, _u64, _u64, _vp, _vp, _vp, _vp,
+                           _sz, _vp], _int),
     "fs_logits_gemm": ([_vp, _vp, _i64, _i64, _i64, _vp, _int, _vp], _int),
     "fs_sample_from_logits": ([_vp, _int, _i64, _i64, _f32, _vp, _u64, _u64, _u32, _vp, _vp, _vp,
                                _sz, _vp], _int),
@@ -188,6 +190,25 @@ def fs_sample_ex(H, W, temperature=1.0, seed=0, offset=0, flags=0, out_idx=None,
                               _ptr(out_idx), _ptr(out_score), _ptr(out_logits), _ptr(ws),
                               ws.numel(), _stream(stream)))
     return out_idx, out_score, out_logits
+
+
+def fs_sample_logprob(H, W, temperature=1.0, seed=0, offset=0, out_idx=None, out_score=None,
+                      out_logprob=None, ws=None, want_score=True, stream=None):
+    """fs_sample_ex plus the sampled token's log-probability.  Returns (idx, score, logprob)."""
+    _check_matrix("H", H, torch.bfloat16)
+    _check_matrix("W", W, torch.bfloat16)
+    B, D = H.shape
+    V = W.shape[0]
+    T, Tv = _temps(temperature, H.device)
+    out_idx, out_score = _outs(B, H.device, out_idx, out_score, want_score)
+    if out_logprob is None:
+        out_logprob = torch.empty(B, dtype=torch.float32, device=H.device)
+    if ws is None:
+        ws = workspace(B, V, D, H.device)
+    _check(lib().fs_sample_logprob(_ptr(H), _ptr(W), B, V, D, T, _ptr(Tv), seed, offset,
+                                   _ptr(out_idx), _ptr(out_score), _ptr(out_logprob), _ptr(ws),
+                                   ws.numel(), _stream(stream)))
+    return out_idx, out_score, out_logprob
 
 
 def fs_stage1(H, W, ws, temperature=1.0, seed=0, offset=0, flags=0, out_logits=None,

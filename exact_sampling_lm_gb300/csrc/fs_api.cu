@@ -54,6 +54,8 @@ static fs_status cuda_fail(cudaError_t e, const char *what) {
 // that each CTA streams a 1/P share of W once.  CTA c takes batch tile c % nM
 // and partition c / nM: the nM CTAs that share a partition run side by side
 // and read the same W tiles, so W comes from HBM about once.
+constexpr int kWorkspaceRegions = 5;
+
 bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *p) {
     if (B < 1 || V < 1 || D < 1 || num_sms < 1) return false;
     p->B = B;
@@ -83,16 +85,30 @@ bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *p) {
     p->nChunks = static_cast<int>((V + kLogitsChunk - 1) / kLogitsChunk);
     const int64_t slots = p->nCand > p->nChunks ? p->nCand : p->nChunks;
     const int64_t region = ((slots * B * 4) + 255) / 256 * 256;
-    p->wsBytes = static_cast<size_t>(2 * region);
+    p->wsBytes = static_cast<size_t>(kWorkspaceRegions * region);
     return true;
 }
 
-// Candidate buffers inside a workspace: scores, then indices.
-static void split_workspace(const Plan &p, void *ws, float **score, int32_t **idx) {
+// Candidate buffers inside a workspace, each [slots][B] of 4-byte values:
+// score, index, and (log-probability calls only) the winner's l~ and the
+// log-mass pair (max, sum).
+struct Candidates {
+    float *score;
+    int32_t *idx;
+    float *lt, *m, *s;
+};
+
+static Candidates split_workspace(const Plan &p, void *ws) {
     const int64_t slots = p.nCand > p.nChunks ? p.nCand : p.nChunks;
     const int64_t region = ((slots * p.B * 4) + 255) / 256 * 256;
-    *score = static_cast<float *>(ws);
-    *idx = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + region);
+    char *base = static_cast<char *>(ws);
+    Candidates c;
+    c.score = reinterpret_cast<float *>(base);
+    c.idx = reinterpret_cast<int32_t *>(base + region);
+    c.lt = reinterpret_cast<float *>(base + 2 * region);
+    c.m = reinterpret_cast<float *>(base + 3 * region);
+    c.s = reinterpret_cast<float *>(base + 4 * region);
+    return c;
 }
 
 // ------------------------------------------------------------------ device info
@@ -227,8 +243,7 @@ static uint64_t wait_timeout_ns() {
 static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &p,
                             float temperature, const float *temperatures, uint64_t seed,
                             uint64_t offset, uint32_t flags, float *out_logits, void *out_y,
-                            int y_dtype, float *cand_score, int32_t *cand_idx,
-                            cudaStream_t stream) {
+                            int y_dtype, const Candidates *cand, cudaStream_t stream) {
     CUtensorMap tmH, tmW64, tmW16;
     fs_status st;
     // With one batch tile, load only the live rows of H (rounded up to the
@@ -250,8 +265,11 @@ static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &
     a.seed = seed;
     a.offset = offset;
     a.flags = flags;
-    a.cand_score = cand_score;
-    a.cand_idx = cand_idx;
+    a.cand_score = cand ? cand->score : nullptr;
+    a.cand_idx = cand ? cand->idx : nullptr;
+    a.cand_lt = cand ? cand->lt : nullptr;
+    a.cand_m = cand ? cand->m : nullptr;
+    a.cand_s = cand ? cand->s : nullptr;
     a.out_logits = out_logits;
     a.out_y = out_y;
     const void *dst = out_logits ? static_cast<const void *>(out_logits) : out_y;
@@ -351,12 +369,10 @@ fs_status fs_stage1(const void *H, const void *W, int64_t B, int64_t V, int64_t 
     Plan p;
     make_plan(B, V, D, info.sms, &p);
     if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
-    float *cs;
-    int32_t *ci;
-    split_workspace(p, workspace, &cs, &ci);
+    const Candidates cand = split_workspace(p, workspace);
     const int mode = (flags & FS_FLAG_STORE_LOGITS) ? kModeSampleStore : kModeSample;
     return run_stage1(mode, H, W, p, temperature, temperatures, seed, offset, flags,
-                      (flags & FS_FLAG_STORE_LOGITS) ? out_logits : nullptr, nullptr, 0, cs, ci,
+                      (flags & FS_FLAG_STORE_LOGITS) ? out_logits : nullptr, nullptr, 0, &cand,
                       static_cast<cudaStream_t>(stream));
 }
 
@@ -373,11 +389,9 @@ fs_status fs_stage2(int64_t B, int64_t V, int64_t D, float temperature,
     Plan p;
     make_plan(B, V, D, info.sms, &p);
     if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
-    float *cs;
-    int32_t *ci;
-    split_workspace(p, const_cast<void *>(workspace), &cs, &ci);
-    cudaError_t e = launch_stage2(cs, ci, p.nCand, B, temperatures, temperature, out_idx,
-                                  out_score, static_cast<cudaStream_t>(stream));
+    const Candidates cand = split_workspace(p, const_cast<void *>(workspace));
+    cudaError_t e = launch_stage2(cand.score, cand.idx, p.nCand, B, temperatures, temperature,
+                                  out_idx, out_score, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "Stage 2 launch");
     return FS_OK;
 }
@@ -413,6 +427,34 @@ fs_status fs_sample(const void *H, const void *W, int64_t B, int64_t V, int64_t 
                         out_score, nullptr, ws, p.wsBytes, stream);
 }
 
+fs_status fs_sample_logprob(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                            float temperature, const float *temperatures, uint64_t seed,
+                            uint64_t offset, int64_t *out_idx, float *out_score,
+                            float *out_logprob, void *workspace, size_t ws_bytes,
+                            void *stream) {
+    fs_status st;
+    if ((st = validate_gemm_inputs(H, W, B, V, D)) != FS_OK) return st;
+    if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
+    if (!out_idx || !out_logprob)
+        return fail(FS_ERR_INVALID_ARG, "out_idx and out_logprob must be non-null");
+    int dev;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    Plan p;
+    make_plan(B, V, D, info.sms, &p);
+    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    const Candidates cand = split_workspace(p, workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = run_stage1(kModeSampleLogprob, H, W, p, temperature, temperatures, seed, offset, 0,
+                         nullptr, nullptr, 0, &cand, s)) != FS_OK)
+        return st;
+    cudaError_t e = launch_stage2_logprob(cand.score, cand.idx, cand.lt, cand.m, cand.s, p.nCand,
+                                          B, temperatures, temperature, out_idx, out_score,
+                                          out_logprob, s);
+    if (e != cudaSuccess) return cuda_fail(e, "Stage 2 (log-probability) launch");
+    return FS_OK;
+}
+
 fs_status fs_logits_gemm(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
                          void *Y, int y_dtype, void *stream) {
     fs_status st;
@@ -426,7 +468,7 @@ fs_status fs_logits_gemm(const void *H, const void *W, int64_t B, int64_t V, int
     Plan p;
     make_plan(B, V, D, info.sms, &p);
     return run_stage1(y_dtype == FS_DTYPE_F32 ? kModeGemmF32 : kModeGemmBf16, H, W, p, 1.0f,
-                      nullptr, 0, 0, 0, nullptr, Y, y_dtype, nullptr, nullptr,
+                      nullptr, 0, 0, 0, nullptr, Y, y_dtype, nullptr,
                       static_cast<cudaStream_t>(stream));
 }
 
@@ -450,14 +492,13 @@ fs_status fs_sample_from_logits(const void *Y, int y_dtype, int64_t B, int64_t V
     Plan p;
     make_plan(B, V, 8, info.sms, &p);
     if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
-    float *cs;
-    int32_t *ci;
-    split_workspace(p, workspace, &cs, &ci);
+    const Candidates cand = split_workspace(p, workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_logits_sample(Y, y_dtype, B, V, temperatures, temperature, seed,
-                                         offset, flags, cs, ci, p.nChunks, s);
+                                         offset, flags, cand.score, cand.idx, p.nChunks, s);
     if (e != cudaSuccess) return cuda_fail(e, "logits sampling launch");
-    e = launch_stage2(cs, ci, p.nChunks, B, temperatures, temperature, out_idx, out_score, s);
+    e = launch_stage2(cand.score, cand.idx, p.nChunks, B, temperatures, temperature, out_idx,
+                      out_score, s);
     if (e != cudaSuccess) return cuda_fail(e, "Stage 2 launch");
     return FS_OK;
 }

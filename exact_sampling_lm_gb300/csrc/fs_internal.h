@@ -26,7 +26,7 @@ constexpr int kWarpTma = kNumEpiWarps;            // warp 16
 constexpr int kWarpMma = kNumEpiWarps + 1;        // warp 17
 constexpr int kThreads = (kNumEpiWarps + 2) * 32; // 576
 constexpr int kTmemCols = 512;  // two 256-column accumulators
-constexpr int kCombineBytes = kColParts * kBM * 8;  // per-row bests of the column parts
+constexpr int kCombineBytes = kColParts * kBM * 20;  // per-row results of the column parts
 constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 1024 + 256 + kCombineBytes;
 constexpr int kFinalTileUnits = 8;  // last tile of a partition: 128 rows
 constexpr int kUnitRows = 16;  // vocabulary partitions are multiples of 16 rows
@@ -40,6 +40,7 @@ enum Stage1Mode : int {
     kModeSampleStore = 1,  // same, plus f32 logits written to HBM
     kModeGemmBf16 = 2,     // unfused GEMM: Y written as bf16, no sampling
     kModeGemmF32 = 3,      // unfused GEMM: Y written as f32, no sampling
+    kModeSampleLogprob = 4,  // fused sampling plus the online log-mass of each row
 };
 
 struct Plan {
@@ -66,6 +67,9 @@ struct Stage1Args {
     uint32_t flags;
     float *cand_score;  // [nCand][B]
     int32_t *cand_idx;  // [nCand][B]
+    float *cand_lt;     // [nCand][B] winner's l*invT          (kModeSampleLogprob)
+    float *cand_m;      // [nCand][B] running max of l*invT      (kModeSampleLogprob)
+    float *cand_s;      // [nCand][B] sum of exp(l*invT - max)  (kModeSampleLogprob)
     float *out_logits;  // [B][V] f32 (kModeSampleStore)
     void *out_y;        // [B][V] bf16/f32 (GEMM modes)
     int y_vec_ok;       // row starts of Y / out_logits are 16-byte aligned
@@ -80,6 +84,13 @@ cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const CUtensorMap &t
 cudaError_t launch_stage2(const float *cand_score, const int32_t *cand_idx, int nCand,
                           int64_t B, const float *temps, float temp_scalar, int64_t *out_idx,
                           float *out_score, cudaStream_t stream);
+
+// Stage 2 with the log-mass merge: also writes out_logprob [B].
+cudaError_t launch_stage2_logprob(const float *cand_score, const int32_t *cand_idx,
+                                  const float *cand_lt, const float *cand_m, const float *cand_s,
+                                  int nCand, int64_t B, const float *temps, float temp_scalar,
+                                  int64_t *out_idx, float *out_score, float *out_logprob,
+                                  cudaStream_t stream);
 
 cudaError_t launch_logits_sample(const void *Y, int y_dtype, int64_t B, int64_t V,
                                  const float *temps, float temp_scalar, uint64_t seed,

@@ -91,6 +91,93 @@ cudaError_t launch_stage2(const float *cand_score, const int32_t *cand_idx, int 
                               temp_scalar, out_idx, out_score);
 }
 
+// ------------------------------------------------------------------ Stage 2 with log-mass
+// Besides the argmax, each row merges the partitions' log-masses
+// (m_j, s_j) = (max l~, sum exp(l~ - max)) over the finite l~ into
+// (M, S) and returns log p(idx) = (l~[idx] - M) - log S, the log-probability
+// of the sampled token under softmax(l~) (the grouped variant's "local
+// log-mass" summaries, reduced over the whole vocabulary).
+__device__ __forceinline__ void lse_merge_acc(float &m, float &s, float m2, float s2) {
+    if (!(s2 > 0.0f)) return;
+    if (m2 > m) {
+        s = s * expf(m - m2) + s2;
+        m = m2;
+    } else {
+        s += s2 * expf(m2 - m);
+    }
+}
+
+__global__ void __launch_bounds__(kStage2Warps * 32)
+    stage2_logprob_kernel(const float *__restrict__ cand_score,
+                          const int32_t *__restrict__ cand_idx, const float *__restrict__ cand_lt,
+                          const float *__restrict__ cand_m, const float *__restrict__ cand_s,
+                          int nCand, int64_t B, const float *__restrict__ temps,
+                          float temp_scalar, int64_t *__restrict__ out_idx,
+                          float *__restrict__ out_score, float *__restrict__ out_logprob) {
+    griddep_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t b = static_cast<int64_t>(blockIdx.x) * kStage2Warps + (threadIdx.x >> 5);
+    if (b >= B) return;
+    float best = -INFINITY, blt = __int_as_float(0x7fc00000);
+    uint32_t bi = 0xFFFFFFFFu;
+    float m = -INFINITY, sum = 0.0f;
+    for (int i = lane; i < nCand; i += 32) {
+        const int64_t o = static_cast<int64_t>(i) * B + b;
+        const float sc = cand_score[o];
+        const uint32_t id = static_cast<uint32_t>(cand_idx[o]);
+        if (better(sc, id, best, bi)) {
+            best = sc;
+            bi = id;
+            blt = cand_lt[o];
+        }
+        lse_merge_acc(m, sum, cand_m[o], cand_s[o]);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        const float sc = __shfl_xor_sync(0xffffffffu, best, d);
+        const uint32_t id = __shfl_xor_sync(0xffffffffu, bi, d);
+        const float lt2 = __shfl_xor_sync(0xffffffffu, blt, d);
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, d);
+        const float s2 = __shfl_xor_sync(0xffffffffu, sum, d);
+        if (better(sc, id, best, bi)) {
+            best = sc;
+            bi = id;
+            blt = lt2;
+        }
+        lse_merge_acc(m, sum, m2, s2);
+    }
+    if (lane == 0) {
+        const float T = temps ? temps[b] : temp_scalar;
+        const bool ok = temperature_ok(T);
+        const bool found = ok && bi != 0xFFFFFFFFu;
+        out_idx[b] = found ? static_cast<int64_t>(bi) : -1;
+        if (out_score) out_score[b] = ok ? best : __int_as_float(0x7fc00000);
+        const bool lp_ok = found && isfinite(blt) && sum > 0.0f;
+        out_logprob[b] = lp_ok ? (blt - m) - logf(sum) : __int_as_float(0x7fc00000);
+    }
+}
+
+cudaError_t launch_stage2_logprob(const float *cand_score, const int32_t *cand_idx,
+                                  const float *cand_lt, const float *cand_m, const float *cand_s,
+                                  int nCand, int64_t B, const float *temps, float temp_scalar,
+                                  int64_t *out_idx, float *out_score, float *out_logprob,
+                                  cudaStream_t stream) {
+    const int64_t blocks = (B + kStage2Warps - 1) / kStage2Warps;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kStage2Warps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, stage2_logprob_kernel, cand_score, cand_idx, cand_lt, cand_m,
+                              cand_s, nCand, B, temps, temp_scalar, out_idx, out_score,
+                              out_logprob);
+}
+
 // ------------------------------------------------------------------ unfused sampling pass
 // Block (chunk, row): 256 threads scan kLogitsChunk logits of one row, 8 per
 // thread per step (one Philox call), then reduce to one candidate.

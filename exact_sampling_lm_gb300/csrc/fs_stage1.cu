@@ -133,6 +133,32 @@ __device__ __forceinline__ uint32_t pick16x(const uint32_t (&a)[8], const uint32
     return r;
 }
 
+// exp(x) from the hardware exp2 (relative error about 2^-22): the log-mass
+// is a sum of positive terms, so this error does not accumulate.
+__device__ __forceinline__ float exp2_approx_scaled(float x) {
+    return ex2_approx(x * 1.4426950408889634f);
+}
+
+// Online log-sum-exp: add a finite element x to (m, s) = (max, sum exp(. - max)).
+__device__ __forceinline__ void lse_add(float &m, float &s, float x) {
+    if (x > m) {
+        s = s * exp2_approx_scaled(m - x) + 1.0f;
+        m = x;
+    } else {
+        s += exp2_approx_scaled(x - m);
+    }
+}
+
+// Merge (m2, s2) into (m, s); an empty pair has m = -inf and s = 0.
+__device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2) {
+    if (m2 > m) {
+        s = s * exp2_approx_scaled(m - m2) + s2;
+        m = m2;
+    } else if (s2 > 0.0f) {
+        s += s2 * exp2_approx_scaled(m2 - m);
+    }
+}
+
 __device__ __forceinline__ void epilogue_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(kNumEpiWarps * 32) : "memory");
 }
@@ -192,7 +218,9 @@ template <int MODE, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW64,
                   const __grid_constant__ CUtensorMap tmW16, const Stage1Args a) {
-    constexpr bool kSample = (MODE == kModeSample || MODE == kModeSampleStore);
+    constexpr bool kSample =
+        (MODE == kModeSample || MODE == kModeSampleStore || MODE == kModeSampleLogprob);
+    constexpr bool kLogprob = (MODE == kModeSampleLogprob);
     constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CS) - 1u);
 
     extern __shared__ uint8_t smem_raw[];
@@ -210,6 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *comb_s = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 256);
     int *comb_i = reinterpret_cast<int *>(comb_s + kColParts * kBM);
+    float *comb_lt = reinterpret_cast<float *>(comb_i + kColParts * kBM);
+    float *comb_m = comb_lt + kColParts * kBM;
+    float *comb_sum = comb_m + kColParts * kBM;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -389,6 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const PhiloxRow prow = philox_row(a.seed, a.offset, static_cast<uint64_t>(b));
         float best = -INFINITY;
         int bidx = -1;
+        // log-mass of the row's elements seen by this thread (kLogprob):
+        // lse_m = max l~, lse_s = sum exp(l~ - lse_m); best_lt = l~ of the best
+        float lse_m = -INFINITY, lse_s = 0.0f, best_lt = NAN;
         bool ok = true;
         // Warps without live rows skip the tile loop (they are not counted by
         // the accumulator-release barrier) and wait at the combine barrier.
@@ -424,7 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (i < n_valid && s > best) {
                                         best = s;
                                         bidx = vbase + i;
+                                        best_lt = s;
                                     }
+                                    if (kLogprob && i < n_valid && isfinite(s)) lse_add(lse_m, lse_s, s);
                                 }
                             } else {
                                 // Both Philox blocks of the chunk first (two
@@ -449,6 +485,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 // against the best known before the chunk (a
                                 // lower bound of the running best); survivors
                                 // are scanned exactly, in order.
+                                if (kLogprob) {
+                                    // online log-sum-exp over the finite l~,
+                                    // rescaled once per chunk
+                                    float cm = -INFINITY;
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i)
+                                        if (i < n_valid && isfinite(lt[i])) cm = fmaxf(cm, lt[i]);
+                                    if (cm > lse_m) {
+                                        lse_s *= exp2_approx_scaled(lse_m - cm);
+                                        lse_m = cm;
+                                    }
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i)
+                                        if (i < n_valid && isfinite(lt[i]))
+                                            lse_s += exp2_approx_scaled(lt[i] - lse_m);
+                                }
                                 const float best0 = best;
                                 const uint32_t kb_a = screen_kbound(best0 - lmax_a);
                                 const uint32_t kb_b = screen_kbound(best0 - lmax_b);
@@ -472,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (s > best) {
                                         best = s;
                                         bidx = vbase + i;
+                                        if (kLogprob) best_lt = pick16(lt, i);
                                     }
                                 }
                             }
@@ -498,6 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // then one candidate per (row, partition).
             comb_s[j * kBM + row] = best;
             comb_i[j * kBM + row] = bidx;
+            if (kLogprob) {
+                comb_lt[j * kBM + row] = best_lt;
+                comb_m[j * kBM + row] = lse_m;
+                comb_sum[j * kBM + row] = lse_s;
+            }
             epilogue_barrier();
             if (j == 0 && row_ok) {
 #pragma unroll
@@ -508,10 +566,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (s == best && static_cast<uint32_t>(i) < static_cast<uint32_t>(bidx))) {
                         best = s;
                         bidx = i;
+                        if (kLogprob) best_lt = comb_lt[jj * kBM + row];
                     }
+                    if (kLogprob)
+                        lse_merge(lse_m, lse_s, comb_m[jj * kBM + row], comb_sum[jj * kBM + row]);
                 }
-                a.cand_score[static_cast<size_t>(part) * a.B + b] = best;
-                a.cand_idx[static_cast<size_t>(part) * a.B + b] = bidx;
+                const size_t o = static_cast<size_t>(part) * a.B + b;
+                a.cand_score[o] = best;
+                a.cand_idx[o] = bidx;
+                if (kLogprob) {
+                    a.cand_lt[o] = best_lt;
+                    a.cand_m[o] = lse_m;
+                    a.cand_s[o] = lse_s;
+                }
             }
         }
     }
@@ -614,6 +681,8 @@ cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const CUtensorMap &t
             case kModeGemmBf16:
                 return launch_mode<kModeGemmBf16, 2>(tmH, tmW64, tmW16, a, grid, stream);
             case kModeGemmF32: return launch_mode<kModeGemmF32, 2>(tmH, tmW64, tmW16, a, grid, stream);
+            case kModeSampleLogprob:
+                return launch_mode<kModeSampleLogprob, 2>(tmH, tmW64, tmW16, a, grid, stream);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -623,6 +692,8 @@ cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const CUtensorMap &t
             return launch_mode<kModeSampleStore, 1>(tmH, tmW64, tmW16, a, grid, stream);
         case kModeGemmBf16: return launch_mode<kModeGemmBf16, 1>(tmH, tmW64, tmW16, a, grid, stream);
         case kModeGemmF32: return launch_mode<kModeGemmF32, 1>(tmH, tmW64, tmW16, a, grid, stream);
+        case kModeSampleLogprob:
+            return launch_mode<kModeSampleLogprob, 1>(tmH, tmW64, tmW16, a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

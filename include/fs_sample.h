@@ -133,6 +133,28 @@ fs_status fs_stage2(int64_t B, int64_t V, int64_t D, float temperature,
                     const void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * fs_sample_logprob -- fs_sample_ex that also returns the log-probability of
+ * each sampled token under softmax(l~), l~ = l * fl(1/T):
+ *   out_logprob[b] = l~[idx] - log sum_v exp(l~[v]).
+ * Stage 1 keeps, besides the per-row maximizer, each partition's log-mass
+ * (max l~, sum exp(l~ - max)) -- the online-normalizer analogy of the method
+ * section and the "local sample and local log-mass" summaries of the grouped /
+ * tensor-parallel variant (Section 4) -- and Stage 2 merges them over the
+ * whole vocabulary.  Elements with a non-finite l~ are left out of the sum; a
+ * row whose sampled l~ is not finite, or with an invalid temperature, gets
+ * NaN.  The logits are never written to HBM.  Costs one exp2 per element on
+ * top of fs_sample.
+ *   out_logprob  device f32 [B] (required)
+ *   workspace    as fs_sample_ex (fs_workspace_size covers this call)
+ * Indices and scores are identical to fs_sample_ex's.
+ * ------------------------------------------------------------------------- */
+fs_status fs_sample_logprob(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                            float temperature, const float *temperatures, uint64_t seed,
+                            uint64_t offset, int64_t *out_idx, float *out_score,
+                            float *out_logprob, void *workspace, size_t ws_bytes,
+                            void *stream);
+
+/* ---------------------------------------------------------------------------
  * Unfused comparator: the baseline the IO model of Section 3 describes, a
  * GEMM that writes the logits Y to HBM followed by a sampling pass that reads
  * them back.  Same noise, temperature and tie rule as the fused path.

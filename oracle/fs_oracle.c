@@ -280,7 +280,9 @@ void oracle_sample(const uint16_t *H, const uint16_t *W, int64_t B, int64_t V,
  * exp(l~[v]), with l~ = fl(l * fl(1/T)) in f32 as in the sampling pass and the
  * log-sum-exp evaluated in fp64 as (l~[idx] - max) - log sum exp(l~ - max).  This is the
  * "local log-mass" summary the grouped / tensor-parallel variant returns per
- * shard, reduced here over the whole vocabulary.  For each row of f32 logits
+ * shard, reduced here over the whole vocabulary.  Reading for non-finite
+ * values (the pages are silent): the log-mass runs over the finite l~ only,
+ * and a sampled token whose l~ is not finite gets NaN.  For each row of f32 logits
  * [B, V]: out[b] = logprob of idx[b] (NaN when idx[b] < 0 or T[b] invalid).
  * ------------------------------------------------------------------------- */
 void oracle_logprob(const float *logits, int64_t B, int64_t V, const float *T,
@@ -293,14 +295,18 @@ void oracle_logprob(const float *logits, int64_t B, int64_t V, const float *T,
         }
         float invT = 1.0f / Tb;
         const float *l = logits + b * V;
+        double win = (double)(l[idx[b]] * invT);
         double mx = -INFINITY;
         for (int64_t v = 0; v < V; ++v) {
             double x = (double)(l[v] * invT);
-            if (x > mx) mx = x;
+            if (isfinite(x) && x > mx) mx = x;
         }
         double sum = 0.0;
-        for (int64_t v = 0; v < V; ++v) sum += exp((double)(l[v] * invT) - mx);
-        out[b] = ((double)(l[idx[b]] * invT) - mx) - log(sum);
+        for (int64_t v = 0; v < V; ++v) {
+            double x = (double)(l[v] * invT);
+            if (isfinite(x)) sum += exp(x - mx);
+        }
+        out[b] = (isfinite(win) && sum > 0.0) ? (win - mx) - log(sum) : NAN;
     }
 }
 

@@ -293,3 +293,58 @@ def test_full_size_sampled_rows(fs, dev, name, B):
     if name == "bigvocab":
         run_and_check(fs, H, W, T, seed, offset, "%s B=%d no-noise" % (name, B),
                       flags=fs.FS_FLAG_NO_NOISE, store=False, rows=rows)
+
+
+# ---------------------------------------------------------------- log-probability (log-mass)
+
+@pytest.mark.parametrize("name,B,V,D", [("tiny", 4, None, None), ("qwen", 33, 20011, 128),
+                                        ("llama3_8b", 64, 30000, 256), ("bigvocab", 200, 26214, 64),
+                                        ("llama3_70b", 256, 9000, 128)])
+def test_logprob_matches_oracle(fs, dev, name, B, V, D):
+    """fs_sample_logprob: same samples as fs_sample_ex, and the sampled token's
+    log-probability within 2 x the logits tolerance / T of the oracle's fp64
+    log-softmax of the same token (a logit error moves both terms)."""
+    W = workloads.make_weights(name, V=V, D=D).to(dev)
+    H = workloads.make_hidden(name, B, D=D).to(dev)
+    T = workloads.make_temperature(name, B, device=dev)
+    seed, offset = workloads.sampling_seed(name, B)
+    idx, score, lp = fs.fs_sample_logprob(H, W, temperature=T, seed=seed, offset=offset)
+    i2, s2, _ = fs.fs_sample_ex(H, W, temperature=T, seed=seed, offset=offset)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, i2) and torch.equal(score, s2)
+    l32 = oracle.logits(bits(H), bits(W)).astype(np.float32)
+    Th = host_T(T, B)
+    o_lp = oracle.logprob(l32, Th, idx.cpu().numpy())
+    g_lp = lp.cpu().numpy().astype(np.float64)
+    err = np.abs(g_lp - o_lp)
+    tol = 2 * LOGIT_TOL / np.minimum(Th, 1.0) + 1e-4
+    assert np.all(err <= tol), "max |d logprob| = %g" % err.max()
+    assert np.all(g_lp <= 1e-6)
+    print("[logprob %s B=%d] max |d| = %.2e" % (name, B, err.max()))
+
+
+def test_logprob_invalid_rows_and_full_size(fs, dev):
+    B, V, D = 9, 4099, 64
+    g = torch.Generator(device="cpu").manual_seed(3)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.2).to(torch.bfloat16).to(dev)
+    T = torch.full((B,), 0.8)
+    T[2] = 0.0
+    T[5] = float("nan")
+    idx, score, lp = fs.fs_sample_logprob(H, W, temperature=T.to(dev), seed=1, offset=2)
+    torch.cuda.synchronize()
+    lp = lp.cpu().numpy()
+    assert np.isnan(lp[2]) and np.isnan(lp[5]) and int(idx[2]) == -1
+    assert np.all(np.isfinite(np.delete(lp, [2, 5])))
+    # full-size decode row sample
+    name, B = "llama3_8b", 64
+    W = workloads.make_weights(name, device=dev)
+    H = workloads.make_hidden(name, B, device=dev)
+    idx, _, lp = fs.fs_sample_logprob(H, W, temperature=1.0, seed=7, offset=0)
+    torch.cuda.synchronize()
+    rows = np.array([0, 17, 63])
+    l32 = oracle.logits(bits(H)[rows], bits(W)).astype(np.float32)
+    o = oracle.logprob(l32, 1.0, idx.cpu().numpy()[rows])
+    err = np.abs(lp.cpu().numpy()[rows] - o)
+    assert np.all(err <= 2 * LOGIT_TOL + 1e-4), err
+    print("[logprob llama3_8b full] max |d| = %.2e" % err.max())

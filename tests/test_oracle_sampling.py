@@ -281,3 +281,15 @@ def test_logprob_probabilities_sum_to_one():
     L = np.broadcast_to(l, (V, V))
     lp = oracle.logprob(L, np.full(V, 0.7, dtype=np.float32), np.arange(V))
     assert abs(np.exp(lp).sum() - 1.0) < 1e-12
+
+
+def test_logprob_leaves_out_non_finite_logits():
+    """Reading for non-finite l~ (the pages are silent): the log-mass runs over
+    the finite entries; a sampled token with a non-finite l~ gets NaN."""
+    l = np.array([0.5, -np.inf, 1.0, np.nan, -0.25, np.inf], dtype=np.float32)
+    L = np.broadcast_to(l, (3, 6))
+    got = oracle.logprob(L, np.ones(3, dtype=np.float32), np.array([0, 2, 5]))
+    finite = np.array([0.5, 1.0, -0.25])
+    ref = scipy.special.log_softmax(finite)
+    assert abs(got[0] - ref[0]) < 1e-12 and abs(got[1] - ref[1]) < 1e-12
+    assert np.isnan(got[2])
