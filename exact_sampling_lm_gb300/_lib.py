@@ -30,6 +30,12 @@ FS_DTYPE_BF16 = 0
 FS_DTYPE_F32 = 1
 
 
+class Transforms(ctypes.Structure):
+    """fs_transforms of include/fs_sample.h."""
+    _fields_ = [("bias", ctypes.c_void_p), ("softcap", ctypes.c_float),
+                ("allow_mask", ctypes.c_void_p), ("mask_words", ctypes.c_int64)]
+
+
 class FSError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__("%s: %s" % (STATUS_NAMES.get(status, status), message))
@@ -52,6 +58,8 @@ SIGNATURES = {
     "fs_stage2": ([_i64, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _sz, _vp], _int),
     "fs_sample_logprob": ([_vp, _vp, _i64, _i64, _i64, _f32, _vp, _u64, _u64, _vp, _vp, _vp, _vp,
                            _sz, _vp], _int),
+    "fs_sample_transformed": ([_vp, _vp, _i64, _i64, _i64, ctypes.c_void_p, _f32, _vp, _u64, _u64,
+                               _u32, _vp, _vp, _vp, _vp, _sz, _vp], _int),
     "fs_logits_gemm": ([_vp, _vp, _i64, _i64, _i64, _vp, _int, _vp], _int),
     "fs_sample_from_logits": ([_vp, _int, _i64, _i64, _f32, _vp, _u64, _u64, _u32, _vp, _vp, _vp,
                                _sz, _vp], _int),
@@ -209,6 +217,29 @@ def fs_sample_logprob(H, W, temperature=1.0, seed=0, offset=0, out_idx=None, out
                                    _ptr(out_idx), _ptr(out_score), _ptr(out_logprob), _ptr(ws),
                                    ws.numel(), _stream(stream)))
     return out_idx, out_score, out_logprob
+
+
+def fs_sample_transformed(H, W, bias=None, softcap=0.0, allow_mask=None, temperature=1.0,
+                          seed=0, offset=0, flags=0, want_logprob=False, out_idx=None,
+                          out_score=None, ws=None, stream=None):
+    """Fused sampling after bias [V] / soft-cap / allowed-token mask [B, words] (uint32 as
+    int32).  Returns (idx, score, logprob or None)."""
+    _check_matrix("H", H, torch.bfloat16)
+    _check_matrix("W", W, torch.bfloat16)
+    B, D = H.shape
+    V = W.shape[0]
+    T, Tv = _temps(temperature, H.device)
+    out_idx, out_score = _outs(B, H.device, out_idx, out_score, True)
+    lp = torch.empty(B, dtype=torch.float32, device=H.device) if want_logprob else None
+    if ws is None:
+        ws = workspace(B, V, D, H.device)
+    tf = Transforms(_ptr(bias), float(softcap), _ptr(allow_mask),
+                    0 if allow_mask is None else int(allow_mask.shape[1]))
+    _check(lib().fs_sample_transformed(_ptr(H), _ptr(W), B, V, D, ctypes.addressof(tf), T,
+                                       _ptr(Tv), seed, offset, flags, _ptr(out_idx),
+                                       _ptr(out_score), _ptr(lp), _ptr(ws), ws.numel(),
+                                       _stream(stream)))
+    return out_idx, out_score, lp
 
 
 def fs_stage1(H, W, ws, temperature=1.0, seed=0, offset=0, flags=0, out_logits=None,

@@ -243,7 +243,8 @@ static uint64_t wait_timeout_ns() {
 static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &p,
                             float temperature, const float *temperatures, uint64_t seed,
                             uint64_t offset, uint32_t flags, float *out_logits, void *out_y,
-                            int y_dtype, const Candidates *cand, cudaStream_t stream) {
+                            int y_dtype, const Candidates *cand, cudaStream_t stream,
+                            const fs_transforms *tf = nullptr) {
     CUtensorMap tmH, tmW64, tmW16;
     fs_status st;
     // With one batch tile, load only the live rows of H (rounded up to the
@@ -277,6 +278,10 @@ static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &
     a.y_vec_ok = dst && (reinterpret_cast<uintptr_t>(dst) % 16 == 0) &&
                  (f32 ? (p.V % 4 == 0) : (p.V % 8 == 0));
     a.h_box_rows = h_box_rows;
+    a.bias = tf ? tf->bias : nullptr;
+    a.softcap = tf ? tf->softcap : 0.0f;
+    a.allow_mask = tf ? tf->allow_mask : nullptr;
+    a.mask_words = tf ? tf->mask_words : 0;
     a.timeout_ns = wait_timeout_ns();
     cudaError_t e = launch_stage1(mode, tmH, tmW64, tmW16, a, p.G, stream);
     if (e != cudaSuccess) return cuda_fail(e, "Stage 1 launch");
@@ -452,6 +457,55 @@ fs_status fs_sample_logprob(const void *H, const void *W, int64_t B, int64_t V, 
                                           B, temperatures, temperature, out_idx, out_score,
                                           out_logprob, s);
     if (e != cudaSuccess) return cuda_fail(e, "Stage 2 (log-probability) launch");
+    return FS_OK;
+}
+
+fs_status fs_sample_transformed(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                                const fs_transforms *tf, float temperature,
+                                const float *temperatures, uint64_t seed, uint64_t offset,
+                                uint32_t flags, int64_t *out_idx, float *out_score,
+                                float *out_logprob, void *workspace, size_t ws_bytes,
+                                void *stream) {
+    fs_status st;
+    if ((st = validate_gemm_inputs(H, W, B, V, D)) != FS_OK) return st;
+    if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
+    if (!tf) return fail(FS_ERR_INVALID_ARG, "tf must be non-null (zero it for no transform)");
+    if (!out_idx) return fail(FS_ERR_INVALID_ARG, "out_idx must be non-null");
+    if (flags & ~FS_FLAG_NO_NOISE)
+        return fail(FS_ERR_INVALID_ARG, "only FS_FLAG_NO_NOISE applies to fs_sample_transformed");
+    if (!isfinite(tf->softcap) || tf->softcap < 0.0f)
+        return fail(FS_ERR_INVALID_ARG, "softcap must be finite and >= 0 (got %g)",
+                    static_cast<double>(tf->softcap));
+    if (tf->bias && reinterpret_cast<uintptr_t>(tf->bias) % 16)
+        return fail(FS_ERR_UNSUPPORTED, "bias must be 16-byte aligned");
+    if (tf->allow_mask) {
+        if (tf->mask_words < (V + 31) / 32)
+            return fail(FS_ERR_INVALID_ARG, "mask_words=%lld < ceil(V/32)=%lld",
+                        static_cast<long long>(tf->mask_words),
+                        static_cast<long long>((V + 31) / 32));
+        if (reinterpret_cast<uintptr_t>(tf->allow_mask) % 4)
+            return fail(FS_ERR_UNSUPPORTED, "allow_mask must be 4-byte aligned");
+    }
+    int dev;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    Plan p;
+    make_plan(B, V, D, info.sms, &p);
+    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    const Candidates cand = split_workspace(p, workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int mode = out_logprob ? kModeSampleXformLogprob : kModeSampleXform;
+    if ((st = run_stage1(mode, H, W, p, temperature, temperatures, seed, offset, flags, nullptr,
+                         nullptr, 0, &cand, s, tf)) != FS_OK)
+        return st;
+    cudaError_t e;
+    if (out_logprob)
+        e = launch_stage2_logprob(cand.score, cand.idx, cand.lt, cand.m, cand.s, p.nCand, B,
+                                  temperatures, temperature, out_idx, out_score, out_logprob, s);
+    else
+        e = launch_stage2(cand.score, cand.idx, p.nCand, B, temperatures, temperature, out_idx,
+                          out_score, s);
+    if (e != cudaSuccess) return cuda_fail(e, "Stage 2 launch");
     return FS_OK;
 }
 

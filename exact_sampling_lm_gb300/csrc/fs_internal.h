@@ -41,6 +41,8 @@ enum Stage1Mode : int {
     kModeGemmBf16 = 2,     // unfused GEMM: Y written as bf16, no sampling
     kModeGemmF32 = 3,      // unfused GEMM: Y written as f32, no sampling
     kModeSampleLogprob = 4,  // fused sampling plus the online log-mass of each row
+    kModeSampleXform = 5,    // fused sampling after bias / soft-cap / token mask
+    kModeSampleXformLogprob = 6,  // both
 };
 
 struct Plan {
@@ -74,6 +76,10 @@ struct Stage1Args {
     void *out_y;        // [B][V] bf16/f32 (GEMM modes)
     int y_vec_ok;       // row starts of Y / out_logits are 16-byte aligned
     int h_box_rows;     // rows of the H tensor-map box (8..128; rows above are not loaded)
+    const float *bias;  // nullable [V], 16-byte aligned          (transform modes)
+    float softcap;      // > 0: l = c * tanh(l / c)              (transform modes)
+    const uint32_t *allow_mask;  // nullable [B][mask_words]     (transform modes)
+    int64_t mask_words;
     uint64_t timeout_ns;
 };
 

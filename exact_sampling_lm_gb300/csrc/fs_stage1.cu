@@ -159,6 +159,49 @@ __device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2
     }
 }
 
+// The deterministic transforms of a 16-column chunk of row b, in place on
+// the raw f32 accumulator bits: l += bias[v]; l = c * tanh(l / c) if c > 0;
+// l = -inf where the row's allowed-token mask has a 0 bit.
+__device__ __forceinline__ void apply_transforms(const Stage1Args &a, int b, int vbase,
+                                                 int n_valid, uint32_t (&r)[16]) {
+    float l[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) l[i] = __uint_as_float(r[i]);
+    if (a.bias != nullptr) {
+        if (n_valid == 16) {
+            const float4 *bp = reinterpret_cast<const float4 *>(a.bias + vbase);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 bb = __ldg(bp + q);
+                l[4 * q] = __fadd_rn(l[4 * q], bb.x);
+                l[4 * q + 1] = __fadd_rn(l[4 * q + 1], bb.y);
+                l[4 * q + 2] = __fadd_rn(l[4 * q + 2], bb.z);
+                l[4 * q + 3] = __fadd_rn(l[4 * q + 3], bb.w);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (i < n_valid) l[i] = __fadd_rn(l[i], __ldg(a.bias + vbase + i));
+        }
+    }
+    if (a.softcap > 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            l[i] = __fmul_rn(a.softcap, tanhf(__fdiv_rn(l[i], a.softcap)));
+    }
+    if (a.allow_mask != nullptr) {
+        // vbase is a multiple of 16: the chunk's 16 bits sit in one word
+        const uint32_t word = __ldg(a.allow_mask + static_cast<int64_t>(b) * a.mask_words +
+                                    (vbase >> 5));
+        const uint32_t bits = word >> (vbase & 31);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (!((bits >> i) & 1u)) l[i] = -INFINITY;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(l[i]);
+}
+
 __device__ __forceinline__ void epilogue_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(kNumEpiWarps * 32) : "memory");
 }
@@ -218,9 +261,11 @@ template <int MODE, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW64,
                   const __grid_constant__ CUtensorMap tmW16, const Stage1Args a) {
-    constexpr bool kSample =
-        (MODE == kModeSample || MODE == kModeSampleStore || MODE == kModeSampleLogprob);
-    constexpr bool kLogprob = (MODE == kModeSampleLogprob);
+    constexpr bool kSample = (MODE == kModeSample || MODE == kModeSampleStore ||
+                              MODE == kModeSampleLogprob || MODE == kModeSampleXform ||
+                              MODE == kModeSampleXformLogprob);
+    constexpr bool kLogprob = (MODE == kModeSampleLogprob || MODE == kModeSampleXformLogprob);
+    constexpr bool kXform = (MODE == kModeSampleXform || MODE == kModeSampleXformLogprob);
     constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CS) - 1u);
 
     extern __shared__ uint8_t smem_raw[];
@@ -450,6 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (MODE == kModeSampleStore && row_ok)
                             store_f32_chunk(a.out_logits + static_cast<size_t>(b) * a.V + vbase,
                                             n_valid, r, a.y_vec_ok != 0);
+                        if (kXform && row_ok && t_ok)
+                            apply_transforms(a, b, vbase, n_valid, r);
                         if (row_ok && t_ok) {
                             if (no_noise) {
 #pragma unroll
@@ -683,6 +730,10 @@ cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const CUtensorMap &t
             case kModeGemmF32: return launch_mode<kModeGemmF32, 2>(tmH, tmW64, tmW16, a, grid, stream);
             case kModeSampleLogprob:
                 return launch_mode<kModeSampleLogprob, 2>(tmH, tmW64, tmW16, a, grid, stream);
+            case kModeSampleXform:
+                return launch_mode<kModeSampleXform, 2>(tmH, tmW64, tmW16, a, grid, stream);
+            case kModeSampleXformLogprob:
+                return launch_mode<kModeSampleXformLogprob, 2>(tmH, tmW64, tmW16, a, grid, stream);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -694,6 +745,10 @@ cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const CUtensorMap &t
         case kModeGemmF32: return launch_mode<kModeGemmF32, 1>(tmH, tmW64, tmW16, a, grid, stream);
         case kModeSampleLogprob:
             return launch_mode<kModeSampleLogprob, 1>(tmH, tmW64, tmW16, a, grid, stream);
+        case kModeSampleXform:
+            return launch_mode<kModeSampleXform, 1>(tmH, tmW64, tmW16, a, grid, stream);
+        case kModeSampleXformLogprob:
+            return launch_mode<kModeSampleXformLogprob, 1>(tmH, tmW64, tmW16, a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -155,6 +155,37 @@ fs_status fs_sample_logprob(const void *H, const void *W, int64_t B, int64_t V, 
                             void *stream);
 
 /* ---------------------------------------------------------------------------
+ * fs_sample_transformed -- the fused path with deterministic transforms
+ * applied to the f32 logits in the Stage 1 epilogue, before the temperature
+ * (method section: Stage 1 "applies deterministic transforms"; the pages do
+ * not list them).  In this order, each rounded to f32:
+ *   l' = l + bias[v]                   bias: nullable device f32 [V], 16-byte aligned
+ *   l' = c * tanh(l' / c)   if c > 0   softcap: logit soft-capping (0 = off)
+ *   l' = -inf               where bit (v & 31) of allow_mask[b * mask_words + (v >> 5)]
+ *                           is 0 (allow_mask: nullable device uint32 [B][mask_words],
+ *                           mask_words >= ceil(V / 32); constrained decoding)
+ * then l~ = l' * fl(1/T), s = l~ + g and the argmax as in fs_sample.
+ *   tf           required; a zero-initialised struct means no transform
+ *   flags        FS_FLAG_NO_NOISE only
+ *   out_logprob  nullable device f32 [B]: as fs_sample_logprob, over l~
+ *   workspace    as fs_sample_ex
+ * A row whose tokens are all masked gets out_idx = -1 and score -inf.
+ * ------------------------------------------------------------------------- */
+typedef struct fs_transforms {
+    const float *bias;
+    float softcap;
+    const uint32_t *allow_mask;
+    int64_t mask_words;
+} fs_transforms;
+
+fs_status fs_sample_transformed(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
+                                const fs_transforms *tf, float temperature,
+                                const float *temperatures, uint64_t seed, uint64_t offset,
+                                uint32_t flags, int64_t *out_idx, float *out_score,
+                                float *out_logprob, void *workspace, size_t ws_bytes,
+                                void *stream);
+
+/* ---------------------------------------------------------------------------
  * Unfused comparator: the baseline the IO model of Section 3 describes, a
  * GEMM that writes the logits Y to HBM followed by a sampling pass that reads
  * them back.  Same noise, temperature and tie rule as the fused path.

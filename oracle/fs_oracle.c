@@ -310,6 +310,30 @@ void oracle_logprob(const float *logits, int64_t B, int64_t V, const float *T,
     }
 }
 
+/* ---------------------------------------------------------------------------
+ * Deterministic transforms applied to the f32 logits before the temperature
+ * (method section: Stage 1 "applies deterministic transforms"; the pages do
+ * not list them -- this library offers the common ones), in this order, each
+ * rounded to f32:
+ *   l' = l + bias[v]                         (bias may be NULL)
+ *   l' = c * tanh(l' / c)      if c > 0      (logit soft-capping)
+ *   l' = -inf                  if mask given and bit (v & 31) of
+ *                              mask[b * mask_words + (v >> 5)] is 0
+ * then the usual l~ = l' * fl(1/T).  In place on logits [B, V].
+ * ------------------------------------------------------------------------- */
+void oracle_transform_logits(float *logits, int64_t B, int64_t V, const float *bias,
+                             float softcap, const uint32_t *mask, int64_t mask_words) {
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t v = 0; v < V; ++v) {
+            float l = logits[b * V + v];
+            if (bias) l = l + bias[v];
+            if (softcap > 0.0f) l = softcap * tanhf(l / softcap);
+            if (mask && !((mask[b * mask_words + (v >> 5)] >> (v & 31)) & 1u)) l = -INFINITY;
+            logits[b * V + v] = l;
+        }
+    }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -54,6 +54,8 @@ def _load():
         lib.oracle_sample.restype = None
         lib.oracle_logprob.argtypes = [vp, i64, i64, vp, vp, vp]
         lib.oracle_logprob.restype = None
+        lib.oracle_transform_logits.argtypes = [vp, i64, i64, vp, ctypes.c_float, vp, i64]
+        lib.oracle_transform_logits.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         _lib = lib
@@ -196,6 +198,20 @@ def sample(H_bits, W_bits, T, seed, offset, flags=0, want_logits=False, nthreads
     return idx, best, second, l64
 
 
+def transform_logits(l32, bias=None, softcap=0.0, mask=None):
+    """Bias, soft-cap and allowed-token mask applied to f32 logits [B, V] (a copy).
+
+    mask: uint32 [B, words] (bit v & 31 of word v >> 5 allows token v) or None.
+    """
+    L = np.array(l32, dtype=np.float32, order="C", copy=True)
+    B, V = L.shape
+    bv = None if bias is None else _c(bias, np.float32)
+    mk = None if mask is None else _c(mask, np.uint32)
+    words = 0 if mk is None else mk.shape[1]
+    _load().oracle_transform_logits(_ptr(L), B, V, _ptr(bv), float(softcap), _ptr(mk), words)
+    return L
+
+
 def logprob(l32, T, idx):
     """log softmax(l~)[idx] per row in fp64, l~ = fl(l * fl(1/T)) (f32 logits [B, V])."""
     L = _c(l32, np.float32)
@@ -207,6 +223,6 @@ def logprob(l32, T, idx):
     return out
 
 
-__all__ = ["logprob", "NO_NOISE", "num_threads", "philox4x64_10", "noise_word", "uniform",
+__all__ = ["transform_logits", "logprob", "NO_NOISE", "num_threads", "philox4x64_10", "noise_word", "uniform",
            "gumbel_from_word", "gumbel", "uniform_block", "gumbel_block", "noise_block", "logits",
            "sample_from_logits", "sample"]

@@ -137,3 +137,22 @@ def test_valid_call_without_a_device_reports_cuda_error():
     UNSUPPORTED) instead of crashing: there is no CPU fallback."""
     st = call_sample()
     assert st in (_lib.FS_ERR_CUDA, _lib.FS_ERR_UNSUPPORTED)
+
+
+def test_transformed_entry_validates():
+    L = _lib.lib()
+    ws = 1 << 20
+    tf = _lib.Transforms(None, -1.0, None, 0)
+    assert L.fs_sample_transformed(16, 16, 4, 64, 64, ctypes.addressof(tf), 1.0, None, 0, 0, 0,
+                                   16, None, None, 16, ws, None) == _lib.FS_ERR_INVALID_ARG
+    tf = _lib.Transforms(8, 0.0, None, 0)  # misaligned bias
+    assert L.fs_sample_transformed(16, 16, 4, 64, 64, ctypes.addressof(tf), 1.0, None, 0, 0, 0,
+                                   16, None, None, 16, ws, None) == _lib.FS_ERR_UNSUPPORTED
+    tf = _lib.Transforms(None, 0.0, 16, 1)  # V=64 needs 2 mask words
+    assert L.fs_sample_transformed(16, 16, 4, 64, 64, ctypes.addressof(tf), 1.0, None, 0, 0, 0,
+                                   16, None, None, 16, ws, None) == _lib.FS_ERR_INVALID_ARG
+    assert L.fs_sample_transformed(16, 16, 4, 64, 64, None, 1.0, None, 0, 0, 0,
+                                   16, None, None, 16, ws, None) == _lib.FS_ERR_INVALID_ARG
+    tf = _lib.Transforms(None, 0.0, None, 0)
+    assert L.fs_sample_transformed(16, 16, 4, 64, 64, ctypes.addressof(tf), 1.0, None, 0, 0, 2,
+                                   16, None, None, 16, ws, None) == _lib.FS_ERR_INVALID_ARG

@@ -348,3 +348,68 @@ def test_logprob_invalid_rows_and_full_size(fs, dev):
     err = np.abs(lp.cpu().numpy()[rows] - o)
     assert np.all(err <= 2 * LOGIT_TOL + 1e-4), err
     print("[logprob llama3_8b full] max |d| = %.2e" % err.max())
+
+
+# ---------------------------------------------------------------- deterministic transforms
+
+def _mask(rng, B, V, keep=0.7):
+    words = (V + 31) // 32 + 1
+    allowed = rng.random((B, words * 32)) < keep
+    bits = np.zeros((B, words), dtype=np.uint64)
+    for k in range(32):
+        bits |= allowed[:, k::32].astype(np.uint64) << np.uint64(k)
+    return bits.astype(np.uint32)
+
+
+@pytest.mark.parametrize("B,V,D,softcap,use_bias,use_mask", [
+    (37, 9001, 128, 0.0, True, False), (64, 40000, 64, 30.0, True, True),
+    (5, 4099, 136, 10.0, False, True), (260, 20011, 64, 0.0, True, True)])
+def test_transforms_match_oracle(fs, dev, B, V, D, softcap, use_bias, use_mask):
+    rng = np.random.default_rng(B + V)
+    g = torch.Generator(device="cpu").manual_seed(B * 5 + V)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * (3.0 / D ** 0.5)).to(torch.bfloat16).to(dev)
+    bias = (rng.standard_normal(V) * 2).astype(np.float32) if use_bias else None
+    mask = _mask(rng, B, V) if use_mask else None
+    T = torch.as_tensor(rng.uniform(0.5, 1.5, B).astype(np.float32))
+    tb = torch.as_tensor(bias).to(dev) if use_bias else None
+    tm = torch.as_tensor(mask.view(np.int32)).to(dev) if use_mask else None
+    idx, score, lp = fs.fs_sample_transformed(H, W, bias=tb, softcap=softcap, allow_mask=tm,
+                                              temperature=T.to(dev), seed=9, offset=4,
+                                              want_logprob=True)
+    torch.cuda.synchronize()
+    l32 = oracle.logits(bits(H), bits(W)).astype(np.float32)
+    lx = oracle.transform_logits(l32, bias, softcap, mask)
+    o_idx, o_best, o_second, _ = oracle.sample_from_logits(lx, T.numpy(), 9, 4)
+    g_idx = idx.cpu().numpy()
+    compare_indices(g_idx, o_idx, o_best, o_second, "transforms B=%d V=%d" % (B, V))
+    same = g_idx == o_idx
+    assert np.all(np.abs(score.cpu().numpy()[same] - o_best[same]) <= 1e-3)
+    if use_mask:
+        words = mask[np.arange(B), g_idx // 32]
+        assert np.all((words >> (g_idx % 32).astype(np.uint32)) & 1), "a masked token was sampled"
+    o_lp = oracle.logprob(lx, T.numpy(), g_idx)
+    err = np.abs(lp.cpu().numpy() - o_lp)
+    assert np.all(err <= 2 * LOGIT_TOL / 0.5 + 1e-4), err.max()
+    print("[transforms B=%d V=%d] max |d logprob| = %.2e" % (B, V, err.max()))
+
+
+def test_zero_transforms_equal_plain_sampling_and_full_mask(fs, dev):
+    B, V, D = 70, 30011, 192
+    g = torch.Generator(device="cpu").manual_seed(77)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.08).to(torch.bfloat16).to(dev)
+    i1, s1, _ = fs.fs_sample_transformed(H, W, temperature=0.9, seed=3, offset=5)
+    i2, s2, _ = fs.fs_sample_ex(H, W, temperature=0.9, seed=3, offset=5)
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2) and torch.equal(s1, s2)
+    words = (V + 31) // 32
+    m = torch.full((B, words), -1, dtype=torch.int32)
+    m[4] = 0  # row 4: every token masked
+    i3, s3, lp3 = fs.fs_sample_transformed(H, W, allow_mask=m.to(dev), temperature=0.9, seed=3,
+                                           offset=5, want_logprob=True)
+    torch.cuda.synchronize()
+    assert int(i3[4]) == -1 and float(s3[4]) == float("-inf") and np.isnan(float(lp3[4]))
+    keep = torch.ones(B, dtype=torch.bool)
+    keep[4] = False
+    assert torch.equal(i3[keep.to(dev)], i1[keep.to(dev)])

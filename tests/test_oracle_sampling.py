@@ -293,3 +293,41 @@ def test_logprob_leaves_out_non_finite_logits():
     ref = scipy.special.log_softmax(finite)
     assert abs(got[0] - ref[0]) < 1e-12 and abs(got[1] - ref[1]) < 1e-12
     assert np.isnan(got[2])
+
+
+# ---------------------------------------------------------------- deterministic transforms
+
+def test_transforms_bias_softcap_mask():
+    """Bias, soft-capping and the allowed-token mask, checked elementwise
+    against numpy float32 arithmetic and bit tests."""
+    rng = np.random.default_rng(41)
+    B, V = 3, 100
+    L = (8 * rng.standard_normal((B, V))).astype(np.float32)
+    bias = rng.standard_normal(V).astype(np.float32)
+    words = 4
+    mask = rng.integers(0, 2**32, size=(B, words), dtype=np.uint64).astype(np.uint32)
+    out = oracle.transform_logits(L, bias, 30.0, mask)
+    want = (L + bias).astype(np.float32)
+    want = (np.float32(30.0) * np.tanh(want / np.float32(30.0))).astype(np.float32)
+    allowed = np.array([[(int(mask[b, v // 32]) >> (v % 32)) & 1 for v in range(V)]
+                        for b in range(B)], dtype=bool)
+    assert np.all(out[~allowed] == -np.inf)
+    assert np.allclose(out[allowed], want[allowed], rtol=2e-7, atol=0)
+    assert np.all(np.abs(out[allowed]) < 30.0)
+    # identity when nothing is set
+    assert np.array_equal(oracle.transform_logits(L), L)
+
+
+def test_masked_tokens_are_never_sampled():
+    rng = np.random.default_rng(43)
+    B, V = 2000, 40
+    L = np.broadcast_to(rng.standard_normal(V).astype(np.float32), (B, V))
+    mask = np.zeros((B, 2), dtype=np.uint32)
+    mask[:, 0] = 0b1010_0000_0000_0000_0000_0000_0001_0110  # tokens 1, 2, 4, 29, 31
+    mask[:, 1] = 1 << 3                                     # token 35
+    out = oracle.transform_logits(L, mask=mask)
+    idx = oracle.sample_from_logits(out, 1.0, 5, 0)[0]
+    assert set(np.unique(idx)) <= {1, 2, 4, 29, 31, 35}
+    counts = np.bincount(idx, minlength=V)[[1, 2, 4, 29, 31, 35]].astype(np.float64)
+    p = scipy.special.softmax(l[[1, 2, 4, 29, 31, 35]].astype(np.float64)) if (l := L[0]) is not None else None
+    assert scipy.stats.chisquare(counts, p * B).pvalue > 0.01
