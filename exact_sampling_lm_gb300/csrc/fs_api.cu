@@ -364,7 +364,7 @@ fs_status fs_stage1(const void *H, const void *W, int64_t B, int64_t V, int64_t 
     fs_status st;
     if ((st = validate_gemm_inputs(H, W, B, V, D)) != FS_OK) return st;
     if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
-    if (flags & ~(FS_FLAG_NO_NOISE | FS_FLAG_STORE_LOGITS))
+    if (flags & ~(FS_FLAG_NO_NOISE | FS_FLAG_STORE_LOGITS | FS_FLAG_TEST_NO_LOADS))
         return fail(FS_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
     if ((flags & FS_FLAG_STORE_LOGITS) && !out_logits)
         return fail(FS_ERR_INVALID_ARG, "FS_FLAG_STORE_LOGITS needs out_logits");

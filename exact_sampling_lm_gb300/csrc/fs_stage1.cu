@@ -342,7 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t issued_mask = 0;      // stages that received at least one load
             uint32_t last_phase_bits = 0;  // phase of the last load per stage
             bool ok = true;
-            for (int t = 0; t < ntiles && ok; ++t) {
+            // test hook (flag 0x100): issue nothing, so the consumers' first
+            // bounded waits expire and the timeout path runs
+            const int ntiles_loaded = (a.flags & 0x100u) ? 0 : ntiles;
+            for (int t = 0; t < ntiles_loaded && ok; ++t) {
                 int v0, tn;
                 tile_geom(geom, t, v0, tn);
                 const int tn16 = round_up16(tn);

@@ -69,6 +69,14 @@ typedef enum fs_status {
                                      out_logits [B, V]: the logits-store flag the  \
                                      IO-model check uses (Section 3)               */
 
+/* Test hook of fs_stage1 / fs_sample_ex: Stage 1's loader issues no loads,
+ * so the first bounded wait of every CTA expires (after FS_WAIT_TIMEOUT_MS,
+ * default 4000 ms, read from the environment once per process); the kernel
+ * then sets the device error word, stops and returns, and
+ * fs_get_device_status reports FS_ERR_TIMEOUT.  Exercises the failure path
+ * without a fault; never use it outside tests. */
+#define FS_FLAG_TEST_NO_LOADS 0x100u
+
 /* dtype codes of materialised logits Y. */
 #define FS_DTYPE_BF16 0
 #define FS_DTYPE_F32 1
