@@ -60,6 +60,9 @@ SIGNATURES = {
                            _sz, _vp], _int),
     "fs_sample_transformed": ([_vp, _vp, _i64, _i64, _i64, ctypes.c_void_p, _f32, _vp, _u64, _u64,
                                _u32, _vp, _vp, _vp, _vp, _sz, _vp], _int),
+    "fs_sample_shard": ([_vp, _vp, _i64, _i64, _i64, _i64, _f32, _vp, _u64, _u64, _vp, _vp, _vp,
+                         _vp, _sz, _vp], _int),
+    "fs_combine_groups": ([_i64, _i64, _vp, _vp, _u64, _u64, _vp, _vp, _vp], _int),
     "fs_logits_gemm": ([_vp, _vp, _i64, _i64, _i64, _vp, _int, _vp], _int),
     "fs_sample_from_logits": ([_vp, _int, _i64, _i64, _f32, _vp, _u64, _u64, _u32, _vp, _vp, _vp,
                                _sz, _vp], _int),
@@ -240,6 +243,38 @@ def fs_sample_transformed(H, W, bias=None, softcap=0.0, allow_mask=None, tempera
                                        _ptr(out_score), _ptr(lp), _ptr(ws), ws.numel(),
                                        _stream(stream)))
     return out_idx, out_score, lp
+
+
+def fs_sample_shard(H, W_shard, vocab_offset, temperature=1.0, seed=0, offset=0, ws=None,
+                    stream=None):
+    """Local sample (global index), score and log-mass of one vocabulary shard.
+    Returns (idx int64 [B], score f32 [B], logmass f32 [B])."""
+    _check_matrix("H", H, torch.bfloat16)
+    _check_matrix("W_shard", W_shard, torch.bfloat16)
+    B, D = H.shape
+    Vs = W_shard.shape[0]
+    T, Tv = _temps(temperature, H.device)
+    idx = torch.empty(B, dtype=torch.int64, device=H.device)
+    score = torch.empty(B, dtype=torch.float32, device=H.device)
+    lm = torch.empty(B, dtype=torch.float32, device=H.device)
+    if ws is None:
+        ws = workspace(B, Vs, D, H.device)
+    _check(lib().fs_sample_shard(_ptr(H), _ptr(W_shard), B, Vs, D, int(vocab_offset), T,
+                                 _ptr(Tv), seed, offset, _ptr(idx), _ptr(score), _ptr(lm),
+                                 _ptr(ws), ws.numel(), _stream(stream)))
+    return idx, score, lm
+
+
+def fs_combine_groups(group_idx, group_logmass, seed=0, offset=0, stream=None):
+    """Grouped sampler over [G, B] local samples / log-masses.  Returns (idx, group)."""
+    G, B = group_idx.shape
+    gi = group_idx.contiguous()
+    gl = group_logmass.contiguous()
+    out = torch.empty(B, dtype=torch.int64, device=gi.device)
+    grp = torch.empty(B, dtype=torch.int64, device=gi.device)
+    _check(lib().fs_combine_groups(G, B, _ptr(gi), _ptr(gl), seed, offset, _ptr(out), _ptr(grp),
+                                   _stream(stream)))
+    return out, grp
 
 
 def fs_stage1(H, W, ws, temperature=1.0, seed=0, offset=0, flags=0, out_logits=None,

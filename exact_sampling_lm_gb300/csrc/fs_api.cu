@@ -244,7 +244,7 @@ static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &
                             float temperature, const float *temperatures, uint64_t seed,
                             uint64_t offset, uint32_t flags, float *out_logits, void *out_y,
                             int y_dtype, const Candidates *cand, cudaStream_t stream,
-                            const fs_transforms *tf = nullptr) {
+                            const fs_transforms *tf = nullptr, int64_t vocab_offset = 0) {
     CUtensorMap tmH, tmW64, tmW16;
     fs_status st;
     // With one batch tile, load only the live rows of H (rounded up to the
@@ -278,6 +278,7 @@ static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &
     a.y_vec_ok = dst && (reinterpret_cast<uintptr_t>(dst) % 16 == 0) &&
                  (f32 ? (p.V % 4 == 0) : (p.V % 8 == 0));
     a.h_box_rows = h_box_rows;
+    a.vocab_offset = vocab_offset;
     a.bias = tf ? tf->bias : nullptr;
     a.softcap = tf ? tf->softcap : 0.0f;
     a.allow_mask = tf ? tf->allow_mask : nullptr;
@@ -506,6 +507,58 @@ fs_status fs_sample_transformed(const void *H, const void *W, int64_t B, int64_t
         e = launch_stage2(cand.score, cand.idx, p.nCand, B, temperatures, temperature, out_idx,
                           out_score, s);
     if (e != cudaSuccess) return cuda_fail(e, "Stage 2 launch");
+    return FS_OK;
+}
+
+fs_status fs_sample_shard(const void *H, const void *W_shard, int64_t B, int64_t V_shard,
+                          int64_t D, int64_t vocab_offset, float temperature,
+                          const float *temperatures, uint64_t seed, uint64_t offset,
+                          int64_t *out_idx, float *out_score, float *out_logmass,
+                          void *workspace, size_t ws_bytes, void *stream) {
+    fs_status st;
+    if ((st = validate_gemm_inputs(H, W_shard, B, V_shard, D)) != FS_OK) return st;
+    if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
+    if (!out_idx || !out_logmass)
+        return fail(FS_ERR_INVALID_ARG, "out_idx and out_logmass must be non-null");
+    if (vocab_offset < 0 || vocab_offset % 16 != 0)
+        return fail(FS_ERR_INVALID_ARG, "vocab_offset=%lld must be >= 0 and a multiple of 16",
+                    static_cast<long long>(vocab_offset));
+    if (vocab_offset + V_shard > FS_MAX_VOCAB)
+        return fail(FS_ERR_UNSUPPORTED, "vocab_offset + V_shard exceeds 2^31-1");
+    int dev;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    Plan p;
+    make_plan(B, V_shard, D, info.sms, &p);
+    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    const Candidates cand = split_workspace(p, workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = run_stage1(kModeSampleLogprob, H, W_shard, p, temperature, temperatures, seed,
+                         offset, 0, nullptr, nullptr, 0, &cand, s, nullptr, vocab_offset)) !=
+        FS_OK)
+        return st;
+    cudaError_t e = launch_stage2_logprob(cand.score, cand.idx, cand.lt, cand.m, cand.s, p.nCand,
+                                          B, temperatures, temperature, out_idx, out_score,
+                                          nullptr, s, out_logmass);
+    if (e != cudaSuccess) return cuda_fail(e, "Stage 2 (shard) launch");
+    return FS_OK;
+}
+
+fs_status fs_combine_groups(int64_t n_groups, int64_t B, const int64_t *group_idx,
+                            const float *group_logmass, uint64_t seed, uint64_t offset,
+                            int64_t *out_idx, int64_t *out_group, void *stream) {
+    if (n_groups < 1 || B < 1)
+        return fail(FS_ERR_INVALID_ARG, "n_groups and B must be >= 1");
+    if (B > FS_MAX_BATCH) return fail(FS_ERR_UNSUPPORTED, "B exceeds 2^24");
+    if (!group_idx || !group_logmass || !out_idx)
+        return fail(FS_ERR_INVALID_ARG, "group_idx, group_logmass and out_idx must be non-null");
+    int dev;
+    DeviceInfo info;
+    fs_status st = device_info(&dev, &info);
+    if (st != FS_OK) return st;
+    cudaError_t e = launch_combine_groups(n_groups, B, group_idx, group_logmass, seed, offset,
+                                          out_idx, out_group, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "group combine launch");
     return FS_OK;
 }
 

@@ -76,6 +76,8 @@ struct Stage1Args {
     void *out_y;        // [B][V] bf16/f32 (GEMM modes)
     int y_vec_ok;       // row starts of Y / out_logits are 16-byte aligned
     int h_box_rows;     // rows of the H tensor-map box (8..128; rows above are not loaded)
+    int64_t vocab_offset;  // global index of W's first row (a multiple of 16): the
+                           // noise and the candidate indices use global indices
     const float *bias;  // nullable [V], 16-byte aligned          (transform modes)
     float softcap;      // > 0: l = c * tanh(l / c)              (transform modes)
     const uint32_t *allow_mask;  // nullable [B][mask_words]     (transform modes)
@@ -91,12 +93,18 @@ cudaError_t launch_stage2(const float *cand_score, const int32_t *cand_idx, int 
                           int64_t B, const float *temps, float temp_scalar, int64_t *out_idx,
                           float *out_score, cudaStream_t stream);
 
-// Stage 2 with the log-mass merge: also writes out_logprob [B].
+// Stage 2 with the log-mass merge: also writes out_logprob [B] and/or the
+// row's log-mass out_logmass [B] (either may be null).
 cudaError_t launch_stage2_logprob(const float *cand_score, const int32_t *cand_idx,
                                   const float *cand_lt, const float *cand_m, const float *cand_s,
                                   int nCand, int64_t B, const float *temps, float temp_scalar,
                                   int64_t *out_idx, float *out_score, float *out_logprob,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, float *out_logmass = nullptr);
+
+// Grouped sampler: per row, the group maximising log-mass + Gumbel (group noise).
+cudaError_t launch_combine_groups(int64_t n_groups, int64_t B, const int64_t *group_idx,
+                                  const float *group_logmass, uint64_t seed, uint64_t offset,
+                                  int64_t *out_idx, int64_t *out_group, cudaStream_t stream);
 
 cudaError_t launch_logits_sample(const void *Y, int y_dtype, int64_t B, int64_t V,
                                  const float *temps, float temp_scalar, uint64_t seed,

@@ -93,6 +93,21 @@ __device__ __forceinline__ void noise_words8(const PhiloxRow &row, uint64_t v8,
     }
 }
 
+// A whole Philox4x64-10 block for an arbitrary counter (used off the hot
+// path: the grouped sampler's draws, counter word 3 = 1).
+__device__ __forceinline__ void philox4x64_10_block(uint64_t c0, uint64_t c1, uint64_t c2,
+                                                    uint64_t c3, uint64_t seed,
+                                                    uint64_t (&w)[4]) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r)
+        philox_round(c0, c1, c2, c3, seed + kPhiloxWeyl0 * static_cast<uint64_t>(r),
+                     kPhiloxWeyl1 * static_cast<uint64_t>(r));
+    w[0] = c0;
+    w[1] = c1;
+    w[2] = c2;
+    w[3] = c3;
+}
+
 // u = ((x >> 8) | 1) * 2^-24: exact in f32, never 0 or 1, symmetric about 1/2.
 __device__ __forceinline__ float uniform_from_word(uint32_t x) {
     return static_cast<float>((x >> 8) | 1u) * 0x1p-24f;

@@ -113,7 +113,8 @@ __global__ void __launch_bounds__(kStage2Warps * 32)
                           const float *__restrict__ cand_m, const float *__restrict__ cand_s,
                           int nCand, int64_t B, const float *__restrict__ temps,
                           float temp_scalar, int64_t *__restrict__ out_idx,
-                          float *__restrict__ out_score, float *__restrict__ out_logprob) {
+                          float *__restrict__ out_score, float *__restrict__ out_logprob,
+                          float *__restrict__ out_logmass) {
     griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t b = static_cast<int64_t>(blockIdx.x) * kStage2Warps + (threadIdx.x >> 5);
@@ -153,7 +154,11 @@ __global__ void __launch_bounds__(kStage2Warps * 32)
         out_idx[b] = found ? static_cast<int64_t>(bi) : -1;
         if (out_score) out_score[b] = ok ? best : __int_as_float(0x7fc00000);
         const bool lp_ok = found && isfinite(blt) && sum > 0.0f;
-        out_logprob[b] = lp_ok ? (blt - m) - logf(sum) : __int_as_float(0x7fc00000);
+        if (out_logprob)
+            out_logprob[b] = lp_ok ? (blt - m) - logf(sum) : __int_as_float(0x7fc00000);
+        if (out_logmass)
+            out_logmass[b] = !ok ? __int_as_float(0x7fc00000)
+                                 : (sum > 0.0f ? m + logf(sum) : -INFINITY);
     }
 }
 
@@ -161,7 +166,7 @@ cudaError_t launch_stage2_logprob(const float *cand_score, const int32_t *cand_i
                                   const float *cand_lt, const float *cand_m, const float *cand_s,
                                   int nCand, int64_t B, const float *temps, float temp_scalar,
                                   int64_t *out_idx, float *out_score, float *out_logprob,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, float *out_logmass) {
     const int64_t blocks = (B + kStage2Warps - 1) / kStage2Warps;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
@@ -175,7 +180,55 @@ cudaError_t launch_stage2_logprob(const float *cand_score, const int32_t *cand_i
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, stage2_logprob_kernel, cand_score, cand_idx, cand_lt, cand_m,
                               cand_s, nCand, B, temps, temp_scalar, out_idx, out_score,
-                              out_logprob);
+                              out_logprob, out_logmass);
+}
+
+// ------------------------------------------------------------------ grouped sampler
+// The pages' grouped variant: every group of the vocabulary has returned a
+// local sample and its log-mass; per row, draw group g with probability
+// proportional to exp(logmass[g]) -- as argmax_g logmass[g] + G_g with
+// Gumbels from Philox4x64-10, key (seed, 0), counter (g >> 3, b, offset, 1)
+// (word 3 = 1 keeps these draws apart from the token noise) -- and return
+// that group's sample.  One thread per row; ties go to the lower g, NaN and
+// -inf never win.
+__global__ void combine_groups_kernel(int64_t n_groups, int64_t B,
+                                      const int64_t *__restrict__ group_idx,
+                                      const float *__restrict__ group_logmass, uint64_t seed,
+                                      uint64_t offset, int64_t *__restrict__ out_idx,
+                                      int64_t *__restrict__ out_group) {
+    const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    float best = -INFINITY;
+    int64_t gbest = -1;
+    for (int64_t g8 = 0; g8 * 8 < n_groups; ++g8) {
+        uint64_t w[4];
+        philox4x64_10_block(static_cast<uint64_t>(g8), static_cast<uint64_t>(b), offset, 1ull,
+                            seed, w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int64_t g = g8 * 8 + e;
+            if (g < n_groups) {
+                const uint32_t x = (e & 1) ? static_cast<uint32_t>(w[e >> 1] >> 32)
+                                           : static_cast<uint32_t>(w[e >> 1]);
+                const float s = __fadd_rn(group_logmass[g * B + b], gumbel_from_word(x));
+                if (s > best) {
+                    best = s;
+                    gbest = g;
+                }
+            }
+        }
+    }
+    out_idx[b] = gbest >= 0 ? group_idx[gbest * B + b] : -1;
+    if (out_group) out_group[b] = gbest;
+}
+
+cudaError_t launch_combine_groups(int64_t n_groups, int64_t B, const int64_t *group_idx,
+                                  const float *group_logmass, uint64_t seed, uint64_t offset,
+                                  int64_t *out_idx, int64_t *out_group, cudaStream_t stream) {
+    const int64_t blocks = (B + 127) / 128;
+    combine_groups_kernel<<<static_cast<unsigned>(blocks), 128, 0, stream>>>(
+        n_groups, B, group_idx, group_logmass, seed, offset, out_idx, out_group);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ unfused sampling pass

@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     const float s = __fmul_rn(__uint_as_float(r[i]), invT);
                                     if (i < n_valid && s > best) {
                                         best = s;
-                                        bidx = vbase + i;
+                                        bidx = static_cast<int>(a.vocab_offset) + vbase + i;
                                         best_lt = s;
                                     }
                                     if (kLogprob && i < n_valid && isfinite(s)) lse_add(lse_m, lse_s, s);
@@ -516,9 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 // Both Philox blocks of the chunk first (two
                                 // independent chains for the scheduler).
                                 uint32_t xa[8], xb[8];
-                                noise_words8(prow, static_cast<uint64_t>(vbase) >> 3, xa);
-                                if (n_valid > 8)
-                                    noise_words8(prow, (static_cast<uint64_t>(vbase) >> 3) + 1, xb);
+                                const uint64_t v8 = static_cast<uint64_t>(a.vocab_offset + vbase) >> 3;
+                                noise_words8(prow, v8, xa);
+                                if (n_valid > 8) noise_words8(prow, v8 + 1, xb);
                                 float lt[16];
                                 float lmax_a = -INFINITY, lmax_b = -INFINITY;
 #pragma unroll
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         __fadd_rn(pick16(lt, i), gumbel_from_word(pick16x(xa, xb, i)));
                                     if (s > best) {
                                         best = s;
-                                        bidx = vbase + i;
+                                        bidx = static_cast<int>(a.vocab_offset) + vbase + i;
                                         if (kLogprob) best_lt = pick16(lt, i);
                                     }
                                 }

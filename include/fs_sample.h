@@ -194,6 +194,42 @@ fs_status fs_sample_transformed(const void *H, const void *W, int64_t B, int64_t
                                 void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Grouped (hierarchical) sampling -- the pages' variant for online and
+ * tensor-parallel settings (abstract; Section 4: each vocabulary shard returns
+ * "a local sample and a local log-mass"), exact by the hierarchical
+ * factorisation P(v) = P(group(v)) P(v | group(v)).
+ *
+ * fs_sample_shard   the fused path over one vocabulary shard W_shard
+ *                   [V_shard, D] whose first row has global index
+ *                   vocab_offset (a multiple of 16): the noise of every
+ *                   element is that of its global index, out_idx holds global
+ *                   indices, and out_logmass [B] (required, device f32) the
+ *                   shard's log sum exp(l~) over its finite l~ (-inf if none,
+ *                   NaN for an invalid T).  out_idx / out_score equal what the
+ *                   unsharded call computes restricted to the shard.
+ * fs_combine_groups per row b, draw group g with probability proportional to
+ *                   exp(group_logmass[g][b]) -- argmax_g of the f32 sum
+ *                   group_logmass[g][b] + G_g, G from Philox4x64-10 with key
+ *                   (seed, 0) and counter (g >> 3, b, offset, 1) (word 3 = 1:
+ *                   apart from the token noise) -- and return
+ *                   out_idx[b] = group_idx[g][b].  group_idx: device int64
+ *                   [n_groups][B]; group_logmass: device f32 [n_groups][B];
+ *                   out_group: nullable device int64 [B].  Ties go to the
+ *                   lower g; NaN and -inf never win (-1 if no group can).
+ * Use the same (seed, offset) in the shard calls and a fresh seed for the
+ * combine.  The result is an exact sample from softmax(l~) over the union of
+ * the shards, but a different one from fs_sample's with the same seed.
+ * ------------------------------------------------------------------------- */
+fs_status fs_sample_shard(const void *H, const void *W_shard, int64_t B, int64_t V_shard,
+                          int64_t D, int64_t vocab_offset, float temperature,
+                          const float *temperatures, uint64_t seed, uint64_t offset,
+                          int64_t *out_idx, float *out_score, float *out_logmass,
+                          void *workspace, size_t ws_bytes, void *stream);
+fs_status fs_combine_groups(int64_t n_groups, int64_t B, const int64_t *group_idx,
+                            const float *group_logmass, uint64_t seed, uint64_t offset,
+                            int64_t *out_idx, int64_t *out_group, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Unfused comparator: the baseline the IO model of Section 3 describes, a
  * GEMM that writes the logits Y to HBM followed by a sampling pass that reads
  * them back.  Same noise, temperature and tie rule as the fused path.

@@ -334,6 +334,109 @@ void oracle_transform_logits(float *logits, int64_t B, int64_t V, const float *b
     }
 }
 
+/* ---------------------------------------------------------------------------
+ * Grouped (hierarchical) sampling, the pages' variant for online and
+ * tensor-parallel settings: each group of the vocabulary returns a local
+ * sample and its local log-mass; a group is drawn with probability
+ * proportional to exp(log-mass), and its local sample is returned.  Exact by
+ * P(v) = P(group(v)) * P(v | group(v)).
+ *
+ * oracle_sample_shard: the local sample of rows [B] over the vocabulary slice
+ * W_shard [Vs, D] whose first row has global index vocab_offset: the full
+ * Gumbel-max pass over the slice with the noise of the global indices, plus
+ * the log-mass log sum exp(l~) over the slice's finite l~ (fp64; -inf if
+ * none; NaN for an invalid T).  out_idx are global indices.
+ *
+ * oracle_combine_groups: per row b, the group g maximising the f32 sum
+ * logmass[g][b] + G(g) (f32 log-masses: the decision is taken in the
+ * kernel's precision), G from Philox4x64-10 with key (seed, 0) and counter
+ * (g >> 3, b, offset, 1) (word 3 = 1 separates these draws from the token
+ * noise), ties to the lower g, NaN / -inf never win; out_idx[b] =
+ * group_idx[g][b] (or -1), out_group[b] = g (or -1), and the two best sums.
+ * ------------------------------------------------------------------------- */
+static uint32_t group_noise_word(uint64_t seed, uint64_t offset, int64_t b, int64_t g) {
+    uint64_t ctr[4] = {(uint64_t)g >> 3, (uint64_t)b, offset, 1};
+    uint64_t key[2] = {seed, 0};
+    uint64_t blk[4];
+    oracle_philox4x64_10(ctr, key, blk);
+    uint64_t w = blk[((uint64_t)g & 7) >> 1];
+    return ((uint64_t)g & 1) ? (uint32_t)(w >> 32) : (uint32_t)(w & 0xFFFFFFFFULL);
+}
+
+float oracle_group_gumbel(uint64_t seed, uint64_t offset, int64_t b, int64_t g) {
+    return oracle_gumbel_from_word(group_noise_word(seed, offset, b, g));
+}
+
+void oracle_sample_shard(const uint16_t *H, const uint16_t *W_shard, int64_t B, int64_t Vs,
+                         int64_t D, int64_t vocab_offset, const float *T, uint64_t seed,
+                         uint64_t offset, int64_t *out_idx, float *out_score,
+                         float *out_second, double *out_logmass, int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+    float *lt = (float *)malloc(sizeof(float) * (size_t)(Vs > 0 ? Vs : 1));
+    for (int64_t b = 0; b < B; ++b) {
+        float Tb = T[b];
+        if (!temperature_ok(Tb)) {
+            out_idx[b] = -1;
+            out_score[b] = NAN;
+            out_second[b] = NAN;
+            out_logmass[b] = NAN;
+            continue;
+        }
+        float invT = 1.0f / Tb;
+        const uint16_t *h = H + b * D;
+        #pragma omp parallel for schedule(static)
+        for (int64_t v = 0; v < Vs; ++v) lt[v] = (float)dot_row(h, W_shard + v * D, D) * invT;
+        float best = -INFINITY, second = -INFINITY;
+        int64_t bi = -1;
+        double mx = -INFINITY;
+        for (int64_t v = 0; v < Vs; ++v) {
+            float s = lt[v] + oracle_gumbel(seed, offset, b, vocab_offset + v);
+            if (s > best) {
+                second = best;
+                best = s;
+                bi = vocab_offset + v;
+            } else if (s > second) {
+                second = s;
+            }
+            if (isfinite(lt[v]) && (double)lt[v] > mx) mx = (double)lt[v];
+        }
+        double sum = 0.0;
+        for (int64_t v = 0; v < Vs; ++v)
+            if (isfinite(lt[v])) sum += exp((double)lt[v] - mx);
+        out_idx[b] = bi;
+        out_score[b] = best;
+        out_second[b] = second;
+        out_logmass[b] = sum > 0.0 ? mx + log(sum) : -INFINITY;
+    }
+    free(lt);
+}
+
+void oracle_combine_groups(int64_t n_groups, int64_t B, const int64_t *group_idx,
+                           const float *group_logmass, uint64_t seed, uint64_t offset,
+                           int64_t *out_idx, int64_t *out_group, float *out_best,
+                           float *out_second) {
+    for (int64_t b = 0; b < B; ++b) {
+        float best = -INFINITY, second = -INFINITY;
+        int64_t gbest = -1;
+        for (int64_t g = 0; g < n_groups; ++g) {
+            float s = group_logmass[g * B + b] + oracle_group_gumbel(seed, offset, b, g);
+            if (s > best) {
+                second = best;
+                best = s;
+                gbest = g;
+            } else if (s > second) {
+                second = s;
+            }
+        }
+        out_group[b] = gbest;
+        out_idx[b] = gbest >= 0 ? group_idx[gbest * B + b] : -1;
+        out_best[b] = best;
+        out_second[b] = second;
+    }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

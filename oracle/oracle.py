@@ -56,6 +56,13 @@ def _load():
         lib.oracle_logprob.restype = None
         lib.oracle_transform_logits.argtypes = [vp, i64, i64, vp, ctypes.c_float, vp, i64]
         lib.oracle_transform_logits.restype = None
+        lib.oracle_group_gumbel.argtypes = [u64, u64, i64, i64]
+        lib.oracle_group_gumbel.restype = ctypes.c_float
+        lib.oracle_sample_shard.argtypes = [vp, vp, i64, i64, i64, i64, vp, u64, u64, vp, vp, vp,
+                                            vp, i32]
+        lib.oracle_sample_shard.restype = None
+        lib.oracle_combine_groups.argtypes = [i64, i64, vp, vp, u64, u64, vp, vp, vp, vp]
+        lib.oracle_combine_groups.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         _lib = lib
@@ -198,6 +205,47 @@ def sample(H_bits, W_bits, T, seed, offset, flags=0, want_logits=False, nthreads
     return idx, best, second, l64
 
 
+def group_gumbel(seed, offset, b, g) -> float:
+    """The Gumbel of group g of row b in the grouped sampler (counter word 3 = 1)."""
+    return float(_load().oracle_group_gumbel(seed, offset, b, g))
+
+
+def sample_shard(H_bits, W_shard_bits, vocab_offset, T, seed, offset, nthreads=0):
+    """Local sample (global index), its score and the local log-mass of a
+    vocabulary slice.  Returns (idx int64 [B], score f32 [B], logmass f64 [B],
+    second f32 [B]) -- second: the slice's runner-up score."""
+    H = _c(H_bits, np.uint16)
+    Ws = _c(W_shard_bits, np.uint16)
+    B, D = H.shape
+    Vs = Ws.shape[0]
+    Tv = _temps(T, B)
+    idx = np.zeros(B, dtype=np.int64)
+    score = np.zeros(B, dtype=np.float32)
+    second = np.zeros(B, dtype=np.float32)
+    lm = np.zeros(B, dtype=np.float64)
+    _load().oracle_sample_shard(_ptr(H), _ptr(Ws), B, Vs, D, int(vocab_offset), _ptr(Tv), seed,
+                                offset, _ptr(idx), _ptr(score), _ptr(second), _ptr(lm), nthreads)
+    return idx, score, lm, second
+
+
+def combine_groups(group_idx, group_logmass, seed, offset, want_scores=False):
+    """Grouped sampler: draw a group by Gumbel-max over the log-masses [G, B]
+    (rounded to f32, the kernel's precision) and return (idx [B], group [B])
+    [, best f32 [B], second f32 [B]]."""
+    gi = _c(group_idx, np.int64)
+    gl = _c(group_logmass, np.float32)
+    G, B = gi.shape
+    out = np.zeros(B, dtype=np.int64)
+    grp = np.zeros(B, dtype=np.int64)
+    best = np.zeros(B, dtype=np.float32)
+    second = np.zeros(B, dtype=np.float32)
+    _load().oracle_combine_groups(G, B, _ptr(gi), _ptr(gl), seed, offset, _ptr(out), _ptr(grp),
+                                  _ptr(best), _ptr(second))
+    if want_scores:
+        return out, grp, best, second
+    return out, grp
+
+
 def transform_logits(l32, bias=None, softcap=0.0, mask=None):
     """Bias, soft-cap and allowed-token mask applied to f32 logits [B, V] (a copy).
 
@@ -223,6 +271,6 @@ def logprob(l32, T, idx):
     return out
 
 
-__all__ = ["transform_logits", "logprob", "NO_NOISE", "num_threads", "philox4x64_10", "noise_word", "uniform",
+__all__ = ["group_gumbel", "sample_shard", "combine_groups", "transform_logits", "logprob", "NO_NOISE", "num_threads", "philox4x64_10", "noise_word", "uniform",
            "gumbel_from_word", "gumbel", "uniform_block", "gumbel_block", "noise_block", "logits",
            "sample_from_logits", "sample"]

@@ -413,3 +413,54 @@ def test_zero_transforms_equal_plain_sampling_and_full_mask(fs, dev):
     keep = torch.ones(B, dtype=torch.bool)
     keep[4] = False
     assert torch.equal(i3[keep.to(dev)], i1[keep.to(dev)])
+
+
+# ---------------------------------------------------------------- grouped sampling / shards
+
+@pytest.mark.parametrize("B,V,D,cuts", [(6, 20000, 64, (4096, 12000)),
+                                        (130, 30011, 96, (16, 20000)),
+                                        (64, 151936, 128, (75968,))])
+def test_shards_and_grouped_combine(fs, dev, B, V, D, cuts):
+    """Each shard's local sample (global indices, global noise) and log-mass
+    match the oracle; merging the shards' candidates by score reproduces the
+    unsharded sample (the pages' candidate exchange); the grouped combine
+    matches the oracle's (group decisions in f32; near-ties counted)."""
+    g = torch.Generator(device="cpu").manual_seed(B * 3 + V)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * (2.0 / D ** 0.5)).to(torch.bfloat16).to(dev)
+    T = (0.6 + torch.rand(B, generator=g)).to(dev)
+    seed, off = 4321, 9
+    bounds = list(zip((0,) + cuts, cuts + (V,)))
+    g_idx, g_sc, g_lm, o_idx, o_sc, o_lm = [], [], [], [], [], []
+    Hb, Th = bits(H), host_T(T, B)
+    for v0, v1 in bounds:
+        i, sc, lm = fs.fs_sample_shard(H, W[v0:v1].contiguous(), v0, temperature=T, seed=seed,
+                                       offset=off)
+        torch.cuda.synchronize()
+        oi, osc, olm, osec = oracle.sample_shard(Hb, bits(W[v0:v1].contiguous()), v0, Th, seed,
+                                                 off)
+        compare_indices(i.cpu().numpy(), oi, osc, osec, "shard [%d,%d)" % (v0, v1))
+        assert np.all(np.abs(lm.cpu().numpy() - olm) <= 2 * LOGIT_TOL / 0.6 + 1e-4)
+        g_idx.append(i); g_sc.append(sc); g_lm.append(lm)
+        o_idx.append(oi); o_sc.append(osc); o_lm.append(olm)
+    # candidate exchange: the best of the shards' candidates is the unsharded sample
+    full_idx, full_sc, _ = fs.fs_sample_ex(H, W, temperature=T, seed=seed, offset=off)
+    S = torch.stack(g_sc)
+    k = torch.argmax(S, dim=0)
+    merged = torch.stack(g_idx)[k, torch.arange(B, device=dev)]
+    torch.cuda.synchronize()
+    diff = (merged != full_idx).cpu().numpy()
+    top2 = torch.topk(S, min(2, len(bounds)), dim=0).values.cpu().numpy()
+    gap = top2[0] - top2[-1] if len(bounds) > 1 else np.full(B, np.inf)
+    assert np.all(gap[diff] < NEAR_TIE), "shard merge differs from the unsharded sample"
+    # grouped combine
+    c_idx, c_grp = fs.fs_combine_groups(torch.stack(g_idx), torch.stack(g_lm), seed=777, offset=off)
+    torch.cuda.synchronize()
+    oc_idx, oc_grp, oc_best, oc_second = oracle.combine_groups(
+        np.stack(o_idx), np.stack(o_lm), 777, off, want_scores=True)
+    grp_near = (oc_best - oc_second) < NEAR_TIE
+    gm = c_grp.cpu().numpy() != oc_grp
+    assert not np.any(gm & ~grp_near), "group choice differs away from a near-tie"
+    same = ~gm
+    assert np.array_equal(c_idx.cpu().numpy()[same], np.stack([x.cpu().numpy() for x in g_idx])[c_grp.cpu().numpy()[same], np.arange(B)[same]])
+    print("[grouped B=%d V=%d] group near-ties %d, mismatches %d" % (B, V, int(grp_near.sum()), int(gm.sum())))

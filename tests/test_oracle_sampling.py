@@ -331,3 +331,61 @@ def test_masked_tokens_are_never_sampled():
     counts = np.bincount(idx, minlength=V)[[1, 2, 4, 29, 31, 35]].astype(np.float64)
     p = scipy.special.softmax(l[[1, 2, 4, 29, 31, 35]].astype(np.float64)) if (l := L[0]) is not None else None
     assert scipy.stats.chisquare(counts, p * B).pvalue > 0.01
+
+
+# ---------------------------------------------------------------- grouped (hierarchical) sampling
+
+def _shard_bounds(V, cuts):
+    b = [0] + list(cuts) + [V]
+    return list(zip(b[:-1], b[1:]))
+
+
+def test_one_group_is_the_plain_sample():
+    """With a single group the grouped sampler returns the plain Gumbel-max
+    sample; a shard's local sample is the global pass restricted to it."""
+    rng = np.random.default_rng(51)
+    B, V, D = 6, 96, 24
+    H = bf16_bits(rng.standard_normal((B, D)))
+    W = bf16_bits(0.3 * rng.standard_normal((V, D)))
+    T = rng.uniform(0.5, 1.5, B).astype(np.float32)
+    idx_full = oracle.sample(H, W, T, 8, 2)[0]
+    i1, s1, lm1, _ = oracle.sample_shard(H, W, 0, T, 8, 2)
+    assert np.array_equal(i1, idx_full)
+    out, grp = oracle.combine_groups(i1[None, :], lm1[None, :], 8, 2)
+    assert np.array_equal(out, idx_full) and np.all(grp == 0)
+    # a shard's log-mass is scipy's logsumexp of its l~
+    l32 = oracle.logits(H, W).astype(np.float32)
+    i2, s2, lm2, _ = oracle.sample_shard(H, W[32:80], 32, T, 8, 2)
+    for b in range(B):
+        lt = (l32[b, 32:80] * (np.float32(1) / T[b])).astype(np.float64)
+        assert abs(lm2[b] - scipy.special.logsumexp(lt)) < 1e-10
+        full_scores = oracle.sample_from_logits(l32[b:b + 1], T[b], 8, 2, want_scores=True,
+                                                row_ids=[b])[3][0]
+        assert i2[b] == 32 + int(np.argmax(full_scores[32:80]))
+
+
+def test_group_noise_is_separate_from_token_noise():
+    a = np.array([oracle.group_gumbel(5, 1, 3, g) for g in range(64)])
+    b = np.array([oracle.gumbel(5, 1, 3, g) for g in range(64)])
+    assert np.count_nonzero(a == b) == 0
+
+
+@pytest.mark.parametrize("cuts", [(16,), (8, 40), (3, 5, 30, 31)])
+def test_grouped_sampler_matches_softmax(cuts):
+    """Hierarchical factorisation: 10^5 grouped draws (rows as trials) follow
+    softmax(l/T) whatever the grouping.  Each group's local sample is the
+    Gumbel-max over the group with the noise of the global indices; its
+    log-mass is scipy's logsumexp of the group's l~."""
+    rng = np.random.default_rng(sum(cuts))
+    V, N, T = 48, 100_000, 0.9
+    l = (1.3 * rng.standard_normal(V)).astype(np.float32)
+    invT = np.float32(1) / np.float32(T)
+    gidx, glm = [], []
+    for v0, v1 in _shard_bounds(V, cuts):
+        _, g = oracle.noise_block(77, 0, 0, N, v0, v1 - v0)
+        lt = (l[v0:v1] * invT).astype(np.float32)
+        gidx.append(v0 + np.argmax((lt[None, :] + g).astype(np.float32), axis=1))
+        glm.append(np.full(N, scipy.special.logsumexp(lt.astype(np.float64))))
+    out, grp = oracle.combine_groups(np.stack(gidx), np.stack(glm), 91, 0)
+    counts = np.bincount(out, minlength=V).astype(np.float64)
+    assert chisq_pvalue(counts, softmax_f32_transform(l, T)) > 0.01
