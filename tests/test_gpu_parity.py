@@ -464,3 +464,58 @@ def test_shards_and_grouped_combine(fs, dev, B, V, D, cuts):
     same = ~gm
     assert np.array_equal(c_idx.cpu().numpy()[same], np.stack([x.cpu().numpy() for x in g_idx])[c_grp.cpu().numpy()[same], np.arange(B)[same]])
     print("[grouped B=%d V=%d] group near-ties %d, mismatches %d" % (B, V, int(grp_near.sum()), int(gm.sum())))
+
+
+# ---------------------------------------------------------------- exactness of the law, edge sizes
+
+def _chisq_p(counts, probs):
+    import scipy.stats
+    exp = probs * counts.sum()
+    small = exp < 5
+    if small.any():
+        counts = np.append(counts[~small], counts[small].sum())
+        exp = np.append(exp[~small], exp[small].sum())
+    return scipy.stats.chisquare(counts, exp).pvalue
+
+
+@pytest.mark.parametrize("V,T", [(64, 0.5), (64, 1.0), (64, 1.5), (2, 1.0), (8, 0.7)])
+def test_gpu_samples_follow_softmax(fs, dev, V, T):
+    """10^5 rows with the same hidden state (so the same logits) draw
+    independent noise; the fused kernel's token frequencies must match
+    softmax(l/T) of those logits (chi-squared, p > 0.01)."""
+    import scipy.special
+    N, D = 100_000, 64
+    g = torch.Generator(device="cpu").manual_seed(V * 10 + int(10 * T))
+    h = torch.randn((1, D), generator=g)
+    H = h.expand(N, D).contiguous().to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.25).to(torch.bfloat16).to(dev)
+    idx, _ = fs.fs_sample(H, W, temperature=T, seed=0xA11CE + V, offset=0)
+    torch.cuda.synchronize()
+    counts = np.bincount(idx.cpu().numpy(), minlength=V).astype(np.float64)
+    l32 = oracle.logits(bits(H[:1]), bits(W)).astype(np.float32)[0]
+    lt = (l32 * (np.float32(1) / np.float32(T))).astype(np.float64)
+    p = _chisq_p(counts, scipy.special.softmax(lt))
+    print("[law V=%d T=%g] p = %.3f" % (V, T, p))
+    assert p > 0.01
+
+
+def test_edge_sizes(fs, dev):
+    """V = 1; a 2^20-row batch; a 2^21-entry vocabulary (indices beyond 2^20)."""
+    g = torch.Generator(device="cpu").manual_seed(99)
+    # V = 1: every valid row samples token 0
+    H = torch.randn((300, 16), generator=g).to(torch.bfloat16).to(dev)
+    W = torch.randn((1, 16), generator=g).to(torch.bfloat16).to(dev)
+    idx, _ = fs.fs_sample(H, W, temperature=1.0, seed=1, offset=0)
+    torch.cuda.synchronize()
+    assert torch.all(idx == 0)
+    # large batch
+    B, V, D = 1 << 20, 40, 64
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.2).to(torch.bfloat16).to(dev)
+    rows = np.array([0, 1, 777, B // 2, B - 2, B - 1])
+    run_and_check(fs, H, W, 0.8, 5, 6, "B=2^20", store=False, rows=rows)
+    # large vocabulary
+    B, V, D = 3, 1 << 21, 16
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.5).to(torch.bfloat16).to(dev)
+    run_and_check(fs, H, W, 1.0, 7, 8, "V=2^21", store=False)
