@@ -494,6 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    r);
                     const int n_valid = min(16, c_hi - c0);
                     const int vbase = v0 + c0;
+                    // warp-wide vote while the warp is converged; lanes without
+                    // a live row keep best = -inf and never block it
+                    const bool first_chunk = __all_sync(0xffffffffu, best == -INFINITY);
                     if (kSample) {
                         if (MODE == kModeSampleStore && row_ok)
                             store_f32_chunk(a.out_logits + static_cast<size_t>(b) * a.V + vbase,
@@ -552,6 +555,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             lse_s += exp2_approx_scaled(lt[i] - lse_m);
                                 }
                                 const float best0 = best;
+                                if (first_chunk) {
+                                    // every lane's best is still -inf: all 16
+                                    // elements would survive the screen, so
+                                    // score them directly
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) {
+                                        const uint32_t xi = i < 8 ? xa[i] : xb[i - 8];
+                                        const float s = __fadd_rn(lt[i], gumbel_from_word(xi));
+                                        if (i < n_valid && s > best) {
+                                            best = s;
+                                            bidx = static_cast<int>(a.vocab_offset) + vbase + i;
+                                            if (kLogprob) best_lt = lt[i];
+                                        }
+                                    }
+                                } else {
                                 const uint32_t kb_a = screen_kbound(best0 - lmax_a);
                                 const uint32_t kb_b = screen_kbound(best0 - lmax_b);
                                 uint32_t pass = 0;
@@ -577,6 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         if (kLogprob) best_lt = pick16(lt, i);
                                     }
                                 }
+                                }  // not a first chunk
                             }
                         }
                     } else if (row_ok) {
