@@ -123,11 +123,14 @@ def _check_matrix(name, t, dtype):
         raise FSError(FS_ERR_INVALID_ARG, "%s must be a contiguous 2-D %s tensor" % (name, dtype))
 
 
-def _temps(temperature, device):
+def _temps(temperature, device, B=None):
     """(scalar, per-row tensor or None) from a float or a [B] f32 CUDA tensor."""
     if isinstance(temperature, torch.Tensor):
         if temperature.dtype != torch.float32 or not temperature.is_cuda:
             raise FSError(FS_ERR_INVALID_ARG, "per-row temperatures must be f32 CUDA")
+        if B is not None and temperature.numel() != B:
+            raise FSError(FS_ERR_INVALID_ARG, "per-row temperatures must have B = %d entries, "
+                          "got %d" % (B, temperature.numel()))
         return 1.0, temperature.contiguous()
     return float(temperature), None
 
@@ -177,7 +180,7 @@ def fs_sample(H, W, temperature=1.0, seed=0, offset=0, out_idx=None, out_score=N
     _check_matrix("W", W, torch.bfloat16)
     B, D = H.shape
     V = W.shape[0]
-    T, Tv = _temps(temperature, H.device)
+    T, Tv = _temps(temperature, H.device, H.shape[0])
     out_idx, out_score = _outs(B, H.device, out_idx, out_score, want_score)
     _check(lib().fs_sample(_ptr(H), _ptr(W), B, V, D, T, _ptr(Tv), seed, offset, _ptr(out_idx),
                            _ptr(out_score), _stream(stream)))
@@ -191,7 +194,7 @@ def fs_sample_ex(H, W, temperature=1.0, seed=0, offset=0, flags=0, out_idx=None,
     _check_matrix("W", W, torch.bfloat16)
     B, D = H.shape
     V = W.shape[0]
-    T, Tv = _temps(temperature, H.device)
+    T, Tv = _temps(temperature, H.device, H.shape[0])
     out_idx, out_score = _outs(B, H.device, out_idx, out_score, want_score)
     if (flags & FS_FLAG_STORE_LOGITS) and out_logits is None:
         out_logits = torch.empty((B, V), dtype=torch.float32, device=H.device)
@@ -210,7 +213,7 @@ def fs_sample_logprob(H, W, temperature=1.0, seed=0, offset=0, out_idx=None, out
     _check_matrix("W", W, torch.bfloat16)
     B, D = H.shape
     V = W.shape[0]
-    T, Tv = _temps(temperature, H.device)
+    T, Tv = _temps(temperature, H.device, H.shape[0])
     out_idx, out_score = _outs(B, H.device, out_idx, out_score, want_score)
     if out_logprob is None:
         out_logprob = torch.empty(B, dtype=torch.float32, device=H.device)
@@ -231,7 +234,7 @@ def fs_sample_transformed(H, W, bias=None, softcap=0.0, allow_mask=None, tempera
     _check_matrix("W", W, torch.bfloat16)
     B, D = H.shape
     V = W.shape[0]
-    T, Tv = _temps(temperature, H.device)
+    T, Tv = _temps(temperature, H.device, H.shape[0])
     out_idx, out_score = _outs(B, H.device, out_idx, out_score, True)
     lp = torch.empty(B, dtype=torch.float32, device=H.device) if want_logprob else None
     if ws is None:
@@ -253,7 +256,7 @@ def fs_sample_shard(H, W_shard, vocab_offset, temperature=1.0, seed=0, offset=0,
     _check_matrix("W_shard", W_shard, torch.bfloat16)
     B, D = H.shape
     Vs = W_shard.shape[0]
-    T, Tv = _temps(temperature, H.device)
+    T, Tv = _temps(temperature, H.device, H.shape[0])
     idx = torch.empty(B, dtype=torch.int64, device=H.device)
     score = torch.empty(B, dtype=torch.float32, device=H.device)
     lm = torch.empty(B, dtype=torch.float32, device=H.device)
@@ -283,13 +286,13 @@ def fs_stage1(H, W, ws, temperature=1.0, seed=0, offset=0, flags=0, out_logits=N
     _check_matrix("W", W, torch.bfloat16)
     B, D = H.shape
     V = W.shape[0]
-    T, Tv = _temps(temperature, H.device)
+    T, Tv = _temps(temperature, H.device, H.shape[0])
     _check(lib().fs_stage1(_ptr(H), _ptr(W), B, V, D, T, _ptr(Tv), seed, offset, flags,
                            _ptr(out_logits), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def fs_stage2(B, V, D, ws, temperature=1.0, out_idx=None, out_score=None, stream=None):
-    T, Tv = _temps(temperature, ws.device)
+    T, Tv = _temps(temperature, ws.device, B)
     _check(lib().fs_stage2(B, V, D, T, _ptr(Tv), _ptr(out_idx), _ptr(out_score), _ptr(ws),
                            ws.numel(), _stream(stream)))
     return out_idx, out_score
@@ -320,7 +323,7 @@ def fs_sample_from_logits(Y, temperature=1.0, seed=0, offset=0, flags=0, out_idx
     if not Y.is_cuda or Y.dim() != 2 or not Y.is_contiguous():
         raise FSError(FS_ERR_INVALID_ARG, "Y must be a contiguous 2-D CUDA tensor")
     B, V = Y.shape
-    T, Tv = _temps(temperature, Y.device)
+    T, Tv = _temps(temperature, Y.device, Y.shape[0])
     out_idx, out_score = _outs(B, Y.device, out_idx, out_score, want_score)
     if ws is None:
         ws = workspace(B, V, 8, Y.device)
@@ -337,7 +340,7 @@ def fs_sample_unfused(H, W, temperature=1.0, seed=0, offset=0, Y=None, y_dtype=F
     _check_matrix("W", W, torch.bfloat16)
     B, D = H.shape
     V = W.shape[0]
-    T, Tv = _temps(temperature, H.device)
+    T, Tv = _temps(temperature, H.device, H.shape[0])
     out_idx, out_score = _outs(B, H.device, out_idx, out_score, want_score)
     if Y is None:
         dt = torch.float32 if y_dtype == FS_DTYPE_F32 else torch.bfloat16
@@ -376,7 +379,7 @@ def fs_sample_noalloc(H, W, temperature=1.0, seed=0, offset=0, out_idx=None, out
     _check_matrix("W", W, torch.bfloat16)
     B, D = H.shape
     V = W.shape[0]
-    T, Tv = _temps(temperature, H.device)
+    T, Tv = _temps(temperature, H.device, H.shape[0])
     out_idx, out_score = _outs(B, H.device, out_idx, out_score, want_score)
     _check(lib().fs_sample_noalloc(_ptr(H), _ptr(W), B, V, D, T, _ptr(Tv), seed, offset,
                                    _ptr(out_idx), _ptr(out_score), _stream(stream)))

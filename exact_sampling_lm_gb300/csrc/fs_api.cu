@@ -211,6 +211,22 @@ static fs_status validate_gemm_inputs(const void *H, const void *W, int64_t B, i
     return FS_OK;
 }
 
+// Device outputs must be aligned to their element size (a misaligned store
+// would fault inside the kernel instead of failing here).
+static fs_status validate_out(const void *p, size_t align, const char *name) {
+    if (p && reinterpret_cast<uintptr_t>(p) % align)
+        return fail(FS_ERR_UNSUPPORTED, "%s must be %zu-byte aligned", name, align);
+    return FS_OK;
+}
+
+static fs_status validate_outputs(const int64_t *out_idx, const float *out_score,
+                                  const float *temperatures) {
+    fs_status st;
+    if ((st = validate_out(out_idx, 8, "out_idx")) != FS_OK) return st;
+    if ((st = validate_out(out_score, 4, "out_score")) != FS_OK) return st;
+    return validate_out(temperatures, 4, "temperatures");
+}
+
 static fs_status validate_temperature(float temperature, const float *temperatures) {
     if (!temperatures && !temperature_ok(temperature))
         return fail(FS_ERR_INVALID_ARG,
@@ -369,6 +385,8 @@ fs_status fs_stage1(const void *H, const void *W, int64_t B, int64_t V, int64_t 
         return fail(FS_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
     if ((flags & FS_FLAG_STORE_LOGITS) && !out_logits)
         return fail(FS_ERR_INVALID_ARG, "FS_FLAG_STORE_LOGITS needs out_logits");
+    if ((st = validate_out(out_logits, 4, "out_logits")) != FS_OK) return st;
+    if ((st = validate_out(temperatures, 4, "temperatures")) != FS_OK) return st;
     int dev;
     DeviceInfo info;
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
@@ -389,6 +407,7 @@ fs_status fs_stage2(int64_t B, int64_t V, int64_t D, float temperature,
     if ((st = validate_shape(B, V, D)) != FS_OK) return st;
     if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
     if (!out_idx) return fail(FS_ERR_INVALID_ARG, "out_idx must be non-null");
+    if ((st = validate_outputs(out_idx, out_score, temperatures)) != FS_OK) return st;
     int dev;
     DeviceInfo info;
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
@@ -421,6 +440,7 @@ fs_status fs_sample(const void *H, const void *W, int64_t B, int64_t V, int64_t 
     if ((st = validate_gemm_inputs(H, W, B, V, D)) != FS_OK) return st;
     if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
     if (!out_idx) return fail(FS_ERR_INVALID_ARG, "out_idx must be non-null");
+    if ((st = validate_outputs(out_idx, out_score, temperatures)) != FS_OK) return st;
     int dev;
     DeviceInfo info;
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
@@ -443,6 +463,8 @@ fs_status fs_sample_logprob(const void *H, const void *W, int64_t B, int64_t V, 
     if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
     if (!out_idx || !out_logprob)
         return fail(FS_ERR_INVALID_ARG, "out_idx and out_logprob must be non-null");
+    if ((st = validate_outputs(out_idx, out_score, temperatures)) != FS_OK) return st;
+    if ((st = validate_out(out_logprob, 4, "out_logprob")) != FS_OK) return st;
     int dev;
     DeviceInfo info;
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
@@ -472,6 +494,8 @@ fs_status fs_sample_transformed(const void *H, const void *W, int64_t B, int64_t
     if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
     if (!tf) return fail(FS_ERR_INVALID_ARG, "tf must be non-null (zero it for no transform)");
     if (!out_idx) return fail(FS_ERR_INVALID_ARG, "out_idx must be non-null");
+    if ((st = validate_outputs(out_idx, out_score, temperatures)) != FS_OK) return st;
+    if ((st = validate_out(out_logprob, 4, "out_logprob")) != FS_OK) return st;
     if (flags & ~FS_FLAG_NO_NOISE)
         return fail(FS_ERR_INVALID_ARG, "only FS_FLAG_NO_NOISE applies to fs_sample_transformed");
     if (!isfinite(tf->softcap) || tf->softcap < 0.0f)
@@ -520,6 +544,8 @@ fs_status fs_sample_shard(const void *H, const void *W_shard, int64_t B, int64_t
     if ((st = validate_temperature(temperature, temperatures)) != FS_OK) return st;
     if (!out_idx || !out_logmass)
         return fail(FS_ERR_INVALID_ARG, "out_idx and out_logmass must be non-null");
+    if ((st = validate_outputs(out_idx, out_score, temperatures)) != FS_OK) return st;
+    if ((st = validate_out(out_logmass, 4, "out_logmass")) != FS_OK) return st;
     if (vocab_offset < 0 || vocab_offset % 16 != 0)
         return fail(FS_ERR_INVALID_ARG, "vocab_offset=%lld must be >= 0 and a multiple of 16",
                     static_cast<long long>(vocab_offset));
@@ -552,6 +578,12 @@ fs_status fs_combine_groups(int64_t n_groups, int64_t B, const int64_t *group_id
     if (B > FS_MAX_BATCH) return fail(FS_ERR_UNSUPPORTED, "B exceeds 2^24");
     if (!group_idx || !group_logmass || !out_idx)
         return fail(FS_ERR_INVALID_ARG, "group_idx, group_logmass and out_idx must be non-null");
+    fs_status st0;
+    if ((st0 = validate_out(group_idx, 8, "group_idx")) != FS_OK ||
+        (st0 = validate_out(group_logmass, 4, "group_logmass")) != FS_OK ||
+        (st0 = validate_out(out_idx, 8, "out_idx")) != FS_OK ||
+        (st0 = validate_out(out_group, 8, "out_group")) != FS_OK)
+        return st0;
     int dev;
     DeviceInfo info;
     fs_status st = device_info(&dev, &info);
@@ -593,6 +625,8 @@ fs_status fs_sample_from_logits(const void *Y, int y_dtype, int64_t B, int64_t V
     if (flags & ~FS_FLAG_NO_NOISE)
         return fail(FS_ERR_INVALID_ARG, "only FS_FLAG_NO_NOISE applies to materialised logits");
     if (!out_idx) return fail(FS_ERR_INVALID_ARG, "out_idx must be non-null");
+    if ((st = validate_outputs(out_idx, out_score, temperatures)) != FS_OK) return st;
+    if ((st = validate_out(Y, y_dtype == FS_DTYPE_F32 ? 4 : 2, "Y")) != FS_OK) return st;
     int dev;
     DeviceInfo info;
     if ((st = device_info(&dev, &info)) != FS_OK) return st;

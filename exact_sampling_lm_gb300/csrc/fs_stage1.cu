@@ -38,6 +38,9 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "fs_internal.h"
 #include "fs_noise.cuh"
 #include "fs_ptx.cuh"
@@ -673,11 +676,11 @@ template <int MODE, int CS>
 static cudaError_t launch_mode(const CUtensorMap &tmH, const CUtensorMap &tmW64,
                                const CUtensorMap &tmW16, const Stage1Args &a, int grid,
                                cudaStream_t stream) {
-    static int configured_mask = 0;  // per device (device ordinals < 32)
+    static std::atomic<uint32_t> configured_mask{0};  // per device (device ordinals < 32)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 32 && !(configured_mask & (1 << dev))) {
+    if (dev >= 32 || !(configured_mask.load() & (1u << dev))) {
         e = cudaFuncSetAttribute(stage1_kernel<MODE, CS>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
@@ -686,7 +689,7 @@ static cudaError_t launch_mode(const CUtensorMap &tmH, const CUtensorMap &tmW64,
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
             if (e != cudaSuccess) return e;
         }
-        configured_mask |= 1 << dev;
+        if (dev < 32) configured_mask.fetch_or(1u << dev);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -706,10 +709,12 @@ static cudaError_t launch_mode(const CUtensorMap &tmH, const CUtensorMap &tmW64,
 // How many 2-CTA clusters of Stage 1 the current device can hold at once
 // (cached per device; 0 if the query fails).
 static int max_pair_clusters() {
+    static std::mutex mu;
     static int cached[64];
     static bool known[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
     if (!known[dev]) {
         int n = 0;
         if (cudaFuncSetAttribute(stage1_kernel<kModeSample, 2>,

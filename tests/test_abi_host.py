@@ -156,3 +156,20 @@ def test_transformed_entry_validates():
     tf = _lib.Transforms(None, 0.0, None, 0)
     assert L.fs_sample_transformed(16, 16, 4, 64, 64, ctypes.addressof(tf), 1.0, None, 0, 0, 2,
                                    16, None, None, 16, ws, None) == _lib.FS_ERR_INVALID_ARG
+
+
+def test_misaligned_outputs_are_rejected():
+    L = _lib.lib()
+    # out_idx must be 8-byte aligned, out_score 4-byte aligned
+    assert L.fs_sample(16, 16, 4, 64, 64, 1.0, None, 0, 0, 20, None, None) == \
+        _lib.FS_ERR_UNSUPPORTED
+    assert L.fs_sample(16, 16, 4, 64, 64, 1.0, None, 0, 0, 16, 18, None) == \
+        _lib.FS_ERR_UNSUPPORTED
+    assert L.fs_sample(16, 16, 4, 64, 64, 1.0, 6, 0, 0, 16, None, None) == \
+        _lib.FS_ERR_UNSUPPORTED
+
+
+def test_binding_checks_per_row_temperature_length():
+    from exact_sampling_lm_gb300 import _lib as b
+    with pytest.raises(b.FSError):
+        b._temps(torch.ones(3), "cpu", 4)  # not CUDA
