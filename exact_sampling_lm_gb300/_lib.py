@@ -50,6 +50,8 @@ _vp, _sz = ctypes.c_void_p, ctypes.c_size_t
 
 SIGNATURES = {
     "fs_sample": ([_vp, _vp, _i64, _i64, _i64, _f32, _vp, _u64, _u64, _vp, _vp, _vp], _int),
+    "fs_sample_host": ([_vp, _vp, _i64, _i64, _i64, _f32, _vp, _u64, _u64, _vp, _vp, _vp],
+                       _int),
     "fs_workspace_size": ([_i64, _i64, _i64], _sz),
     "fs_sample_ex": ([_vp, _vp, _i64, _i64, _i64, _f32, _vp, _u64, _u64, _u32, _vp, _vp, _vp,
                       _vp, _sz, _vp], _int),
@@ -184,6 +186,46 @@ def fs_sample(H, W, temperature=1.0, seed=0, offset=0, out_idx=None, out_score=N
     out_idx, out_score = _outs(B, H.device, out_idx, out_score, want_score)
     _check(lib().fs_sample(_ptr(H), _ptr(W), B, V, D, T, _ptr(Tv), seed, offset, _ptr(out_idx),
                            _ptr(out_score), _stream(stream)))
+    return out_idx, out_score
+
+
+def _check_host(name, t, dtype, dim):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise FSError(FS_ERR_INVALID_ARG, "%s must be a host (CPU) tensor" % name)
+    if t.dtype != dtype or t.dim() != dim or not t.is_contiguous():
+        raise FSError(FS_ERR_INVALID_ARG, "%s must be a contiguous %d-D %s tensor"
+                      % (name, dim, dtype))
+
+
+def fs_sample_host(H_host, W, temperature=1.0, seed=0, offset=0, out_idx=None, out_score=None,
+                   want_score=True, stream=None):
+    """fs_sample with H, per-row temperatures and the outputs in host memory (W on the
+    device).  Outputs are valid once the stream reaches the end of the call; pinned
+    buffers keep the copies asynchronous.  Returns (idx, score) host tensors."""
+    _check_host("H_host", H_host, torch.bfloat16, 2)
+    _check_matrix("W", W, torch.bfloat16)
+    B, D = H_host.shape
+    V = W.shape[0]
+    Tv = None
+    if isinstance(temperature, torch.Tensor):
+        _check_host("temperatures", temperature, torch.float32, 1)
+        if temperature.numel() != B:
+            raise FSError(FS_ERR_INVALID_ARG, "per-row temperatures must have B = %d entries, "
+                          "got %d" % (B, temperature.numel()))
+        T, Tv = 1.0, temperature
+    else:
+        T = float(temperature)
+    if out_idx is None:
+        out_idx = torch.empty(B, dtype=torch.int64).pin_memory()
+    if out_score is None and want_score:
+        out_score = torch.empty(B, dtype=torch.float32).pin_memory()
+    _check_host("out_idx", out_idx, torch.int64, 1)
+    if out_score is not None:
+        _check_host("out_score", out_score, torch.float32, 1)
+    if out_idx.numel() != B or (out_score is not None and out_score.numel() != B):
+        raise FSError(FS_ERR_INVALID_ARG, "outputs must have B = %d entries" % B)
+    _check(lib().fs_sample_host(_ptr(H_host), _ptr(W), B, V, D, T, _ptr(Tv), seed, offset,
+                                _ptr(out_idx), _ptr(out_score), _stream(stream)))
     return out_idx, out_score
 
 

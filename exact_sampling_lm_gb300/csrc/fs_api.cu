@@ -453,6 +453,61 @@ fs_status fs_sample(const void *H, const void *W, int64_t B, int64_t V, int64_t 
                         out_score, nullptr, ws, p.wsBytes, stream);
 }
 
+static size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V, int64_t D,
+                         float temperature, const float *temperatures_host, uint64_t seed,
+                         uint64_t offset, int64_t *out_idx_host, float *out_score_host,
+                         void *stream) {
+    fs_status st;
+    if (!H_host || !W) return fail(FS_ERR_INVALID_ARG, "H_host and W must be non-null");
+    if ((st = validate_shape(B, V, D)) != FS_OK) return st;
+    if (reinterpret_cast<uintptr_t>(W) % 16)
+        return fail(FS_ERR_UNSUPPORTED, "W must be 16-byte aligned");
+    if ((st = validate_temperature(temperature, temperatures_host)) != FS_OK) return st;
+    if (!out_idx_host) return fail(FS_ERR_INVALID_ARG, "out_idx_host must be non-null");
+    int dev;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    Plan p;
+    make_plan(B, V, D, info.sms, &p);
+    // One cached block per (device, stream): the Stage 1 workspace, then the
+    // device copies of H, the temperatures and the outputs.  Calls on one
+    // stream run in order, so the next call's upload cannot overtake this
+    // call's kernels.
+    const size_t ub = static_cast<size_t>(B);
+    const size_t ws_b = round256(p.wsBytes);
+    const size_t h_b = round256(ub * static_cast<size_t>(D) * 2);
+    const size_t t_b = temperatures_host ? round256(ub * 4) : 0;
+    const size_t i_b = round256(ub * 8);
+    const size_t s_b = out_score_host ? round256(ub * 4) : 0;
+    void *blk = nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = cached_workspace(dev, s, ws_b + h_b + t_b + i_b + s_b, &blk)) != FS_OK) return st;
+    char *base = static_cast<char *>(blk);
+    void *ws = base;
+    void *H = base + ws_b;
+    float *T = temperatures_host ? reinterpret_cast<float *>(base + ws_b + h_b) : nullptr;
+    int64_t *idx = reinterpret_cast<int64_t *>(base + ws_b + h_b + t_b);
+    float *score = out_score_host ? reinterpret_cast<float *>(base + ws_b + h_b + t_b + i_b)
+                                  : nullptr;
+    cudaError_t e = cudaMemcpyAsync(H, H_host, ub * static_cast<size_t>(D) * 2,
+                                    cudaMemcpyDefault, s);
+    if (e != cudaSuccess) return cuda_fail(e, "upload of H");
+    if (T && (e = cudaMemcpyAsync(T, temperatures_host, ub * 4, cudaMemcpyDefault, s)) !=
+                 cudaSuccess)
+        return cuda_fail(e, "upload of the temperatures");
+    if ((st = fs_sample_ex(H, W, B, V, D, temperature, T, seed, offset, 0, idx, score, nullptr,
+                           ws, p.wsBytes, stream)) != FS_OK)
+        return st;
+    if ((e = cudaMemcpyAsync(out_idx_host, idx, ub * 8, cudaMemcpyDefault, s)) != cudaSuccess)
+        return cuda_fail(e, "read-back of out_idx");
+    if (score && (e = cudaMemcpyAsync(out_score_host, score, ub * 4, cudaMemcpyDefault, s)) !=
+                     cudaSuccess)
+        return cuda_fail(e, "read-back of out_score");
+    return FS_OK;
+}
+
 fs_status fs_sample_logprob(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
                             float temperature, const float *temperatures, uint64_t seed,
                             uint64_t offset, int64_t *out_idx, float *out_score,

@@ -103,6 +103,32 @@ fs_status fs_sample(const void *H, const void *W, int64_t B, int64_t V, int64_t 
                     float temperature, const float *temperatures, uint64_t seed,
                     uint64_t offset, int64_t *out_idx, float *out_score, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * fs_sample_host -- fs_sample with the per-call data in HOST memory, for a
+ * decode loop whose hidden states and sampled tokens live on the host.  The
+ * weights stay resident on the device (method section: W is read from HBM
+ * once per call).  On `stream`, in order: copy H (and the temperatures) to the
+ * device, Stage 1, Stage 2, copy the indices (and scores) back.
+ *   H_host            host bf16 [B, D], row-major; page-locked memory makes
+ *                     the upload asynchronous (pageable memory is staged by
+ *                     the CUDA runtime before the call returns)
+ *   W                 device bf16 [V, D], row-major, 16-byte aligned
+ *   temperatures_host NULL or host f32 [B]
+ *   out_idx_host      host int64 [B]; valid once the stream has reached the
+ *                     end of this call (cudaStreamSynchronize or an event).
+ *                     With pageable memory the read-back completes before
+ *                     the call returns.
+ *   out_score_host    NULL or host f32 [B], as out_idx_host
+ * The device copies of H, the temperatures and the outputs live in the same
+ * per-(device, stream) cached block as fs_sample's workspace; calls on one
+ * stream reuse it in order.  Host pointers need no particular alignment.
+ * Results are bit-identical to fs_sample on the same data.
+ * ------------------------------------------------------------------------- */
+fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V, int64_t D,
+                         float temperature, const float *temperatures_host, uint64_t seed,
+                         uint64_t offset, int64_t *out_idx_host, float *out_score_host,
+                         void *stream);
+
 /* Bytes of caller workspace that fs_sample_ex, fs_stage1/fs_stage2 and
  * fs_sample_from_logits need for (B, V, D) on the current device.
  * Returns 0 on a bad argument or when no device is visible. */

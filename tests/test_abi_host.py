@@ -173,3 +173,33 @@ def test_binding_checks_per_row_temperature_length():
     from exact_sampling_lm_gb300 import _lib as b
     with pytest.raises(b.FSError):
         b._temps(torch.ones(3), "cpu", 4)  # not CUDA
+
+
+def test_host_buffer_entry_validates():
+    L = _lib.lib()
+    # H_host, W and out_idx_host are required; host pointers need no alignment
+    assert L.fs_sample_host(None, 16, 4, 64, 64, 1.0, None, 0, 0, 16, None, None) == \
+        _lib.FS_ERR_INVALID_ARG
+    assert L.fs_sample_host(16, None, 4, 64, 64, 1.0, None, 0, 0, 16, None, None) == \
+        _lib.FS_ERR_INVALID_ARG
+    assert L.fs_sample_host(16, 16, 4, 64, 64, 1.0, None, 0, 0, None, None, None) == \
+        _lib.FS_ERR_INVALID_ARG
+    assert L.fs_sample_host(16, 8, 4, 64, 64, 1.0, None, 0, 0, 16, None, None) == \
+        _lib.FS_ERR_UNSUPPORTED  # W is the device operand of the TMA loads
+    assert L.fs_sample_host(16, 16, 4, 64, 12, 1.0, None, 0, 0, 16, None, None) == \
+        _lib.FS_ERR_UNSUPPORTED
+    assert L.fs_sample_host(16, 16, 0, 64, 64, 1.0, None, 0, 0, 16, None, None) == \
+        _lib.FS_ERR_INVALID_ARG
+    assert L.fs_sample_host(16, 16, 4, 64, 64, 0.0, None, 0, 0, 16, None, None) == \
+        _lib.FS_ERR_INVALID_ARG
+
+
+def test_host_buffer_binding_rejects_device_or_wrong_tensors():
+    W = torch.zeros(64, 64, dtype=torch.bfloat16)
+    H = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(fs.FSError):  # W must be a CUDA tensor
+        fs.fs_sample_host(H, W)
+    with pytest.raises(fs.FSError):  # H must be bf16
+        fs.fs_sample_host(H.float(), W)
+    with pytest.raises(fs.FSError):  # H must be contiguous
+        fs.fs_sample_host(torch.zeros(64, 4, dtype=torch.bfloat16).t(), W)

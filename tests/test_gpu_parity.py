@@ -218,6 +218,41 @@ def test_side_stream_and_workspace_growth(fs, dev):
         assert torch.equal(idx, ref)
 
 
+def test_host_buffer_entry(fs, dev):
+    """fs_sample_host (H, T and the outputs in host memory) equals fs_sample on
+    device copies bit for bit, with pinned and pageable buffers; back-to-back
+    calls on one stream reuse the staging block in order."""
+    B, V, D = 70, 30011, 192
+    g = torch.Generator(device="cpu").manual_seed(33)
+    Hs = [torch.randn((B, D), generator=g).to(torch.bfloat16) for _ in range(3)]
+    W = (torch.randn((V, D), generator=g) * 0.08).to(torch.bfloat16).to(dev)
+    T = 0.5 + torch.rand(B, generator=g)
+    refs = [fs.fs_sample(H.to(dev), W, temperature=T.to(dev), seed=5, offset=k)
+            for k, H in enumerate(Hs)]
+    pinned = [H.pin_memory() for H in Hs]
+    outs = [fs.fs_sample_host(H, W, temperature=T.pin_memory(), seed=5, offset=k)
+            for k, H in enumerate(pinned)]
+    torch.cuda.synchronize()
+    for (ri, rs), (oi, os_) in zip(refs, outs):
+        assert torch.equal(ri.cpu(), oi) and torch.equal(rs.cpu(), os_)
+    # pageable host memory, scalar temperature, no score
+    i_ref, _ = fs.fs_sample(Hs[0].to(dev), W, temperature=0.9, seed=6, offset=1)
+    idx = torch.empty(B, dtype=torch.int64)
+    fs.fs_sample_host(Hs[0], W, temperature=0.9, seed=6, offset=1, out_idx=idx, want_score=False)
+    torch.cuda.synchronize()
+    assert torch.equal(i_ref.cpu(), idx)
+    # the tiny workload through host buffers against the oracle
+    Wt = workloads.make_weights("tiny", device=dev)
+    Ht = workloads.make_hidden("tiny", 4)
+    seed, offset = workloads.sampling_seed("tiny", 4)
+    ti, ts = fs.fs_sample_host(Ht.pin_memory(), Wt, temperature=1.0, seed=seed, offset=offset)
+    torch.cuda.synchronize()
+    assert fs.fs_get_device_status() == 0
+    o_idx, o_best, o_second, _ = oracle.sample(bits(Ht), bits(Wt), np.ones(4, np.float32),
+                                               seed, offset)
+    compare_indices(ti.numpy(), o_idx, o_best, o_second, "host buffers")
+
+
 # ---------------------------------------------------------------- unfused comparator
 
 @pytest.mark.parametrize("T", [0.8, 1e-3, 0.3, 50.0, "rows"])
