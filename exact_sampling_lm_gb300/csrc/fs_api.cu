@@ -455,6 +455,64 @@ fs_status fs_sample(const void *H, const void *W, int64_t B, int64_t V, int64_t 
 
 static size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
+// The device address of a page-locked host buffer, or nullptr when the buffer
+// is pageable (or not host memory at all).
+static void *mapped_host_alias(void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer is not an error here
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// Per (device, stream) state of fs_sample_host: an internal upload stream,
+// two H / temperature slots used alternately, events that order a slot's
+// upload after the previous reader of that slot, and output staging for
+// pageable host outputs.
+struct HostPath {
+    cudaStream_t copy = nullptr;
+    cudaEvent_t uploaded[2] = {nullptr, nullptr};
+    cudaEvent_t consumed[2] = {nullptr, nullptr};
+    int next = 0;
+    char *block = nullptr;
+    size_t bytes = 0;
+};
+static std::mutex g_host_mu;
+static std::map<std::pair<int, void *>, HostPath> g_host;
+
+static fs_status host_path_ready(HostPath &h, size_t need) {
+    cudaError_t e;
+    if (!h.copy) {
+        if ((e = cudaStreamCreateWithFlags(&h.copy, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e, "cudaStreamCreate(upload stream)");
+        for (int j = 0; j < 2; ++j) {
+            if ((e = cudaEventCreateWithFlags(&h.uploaded[j], cudaEventDisableTiming)) !=
+                    cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&h.consumed[j], cudaEventDisableTiming)) !=
+                    cudaSuccess)
+                return cuda_fail(e, "cudaEventCreate(upload events)");
+        }
+    }
+    if (h.bytes < need) {
+        // cudaFree waits for all work on the device, including reads of the
+        // old block still queued on either stream.
+        if (h.block && (e = cudaFree(h.block)) != cudaSuccess)
+            return cuda_fail(e, "cudaFree(host-path staging)");
+        h.block = nullptr;
+        h.bytes = 0;
+        size_t grow = 65536;
+        while (grow < need) grow <<= 1;
+        if (cudaMalloc(reinterpret_cast<void **>(&h.block), grow) != cudaSuccess) {
+            cudaGetLastError();
+            h.block = nullptr;
+            return fail(FS_ERR_NO_MEMORY, "cudaMalloc(%zu) for host-path staging failed", grow);
+        }
+        h.bytes = grow;
+    }
+    return FS_OK;
+}
+
 fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V, int64_t D,
                          float temperature, const float *temperatures_host, uint64_t seed,
                          uint64_t offset, int64_t *out_idx_host, float *out_score_host,
@@ -471,39 +529,67 @@ fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
     Plan p;
     make_plan(B, V, D, info.sms, &p);
-    // One cached block per (device, stream): the Stage 1 workspace, then the
-    // device copies of H, the temperatures and the outputs.  Calls on one
-    // stream run in order, so the next call's upload cannot overtake this
-    // call's kernels.
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    if ((st = cached_workspace(dev, s, p.wsBytes, &ws)) != FS_OK) return st;
+
+    // Outputs: page-locked host buffers are written by Stage 2 directly;
+    // pageable ones go through device staging and a copy back.
+    int64_t *idx_dev = static_cast<int64_t *>(mapped_host_alias(out_idx_host));
+    float *score_dev = out_score_host ? static_cast<float *>(mapped_host_alias(out_score_host))
+                                      : nullptr;
+    const bool stage_idx = !idx_dev;
+    const bool stage_score = out_score_host && !score_dev;
+
     const size_t ub = static_cast<size_t>(B);
-    const size_t ws_b = round256(p.wsBytes);
-    const size_t h_b = round256(ub * static_cast<size_t>(D) * 2);
+    const size_t h_bytes = ub * static_cast<size_t>(D) * 2;
+    const size_t h_b = round256(h_bytes);
     const size_t t_b = temperatures_host ? round256(ub * 4) : 0;
     const size_t i_b = round256(ub * 8);
-    const size_t s_b = out_score_host ? round256(ub * 4) : 0;
-    void *blk = nullptr;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if ((st = cached_workspace(dev, s, ws_b + h_b + t_b + i_b + s_b, &blk)) != FS_OK) return st;
-    char *base = static_cast<char *>(blk);
-    void *ws = base;
-    void *H = base + ws_b;
-    float *T = temperatures_host ? reinterpret_cast<float *>(base + ws_b + h_b) : nullptr;
-    int64_t *idx = reinterpret_cast<int64_t *>(base + ws_b + h_b + t_b);
-    float *score = out_score_host ? reinterpret_cast<float *>(base + ws_b + h_b + t_b + i_b)
-                                  : nullptr;
-    cudaError_t e = cudaMemcpyAsync(H, H_host, ub * static_cast<size_t>(D) * 2,
-                                    cudaMemcpyDefault, s);
-    if (e != cudaSuccess) return cuda_fail(e, "upload of H");
-    if (T && (e = cudaMemcpyAsync(T, temperatures_host, ub * 4, cudaMemcpyDefault, s)) !=
+    const size_t s_b = round256(ub * 4);
+
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    // Under stream capture the upload stays on the caller's stream (a graph
+    // cannot wait on events recorded outside it); otherwise it runs on the
+    // internal upload stream and overlaps the previous call's kernels.
+    const bool overlap = cap == cudaStreamCaptureStatusNone;
+
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostPath &h = g_host[std::make_pair(dev, static_cast<void *>(s))];
+    if ((st = host_path_ready(h, 2 * (h_b + t_b) + i_b + s_b)) != FS_OK) return st;
+    const int j = h.next;
+    h.next ^= 1;
+    char *slot = h.block + j * (h_b + t_b);
+    void *H = slot;
+    float *T = temperatures_host ? reinterpret_cast<float *>(slot + h_b) : nullptr;
+    if (stage_idx) idx_dev = reinterpret_cast<int64_t *>(h.block + 2 * (h_b + t_b));
+    if (stage_score) score_dev = reinterpret_cast<float *>(h.block + 2 * (h_b + t_b) + i_b);
+
+    cudaStream_t up = overlap ? h.copy : s;
+    if (overlap && (e = cudaStreamWaitEvent(up, h.consumed[j], 0)) != cudaSuccess)
+        return cuda_fail(e, "upload stream wait");
+    if ((e = cudaMemcpyAsync(H, H_host, h_bytes, cudaMemcpyDefault, up)) != cudaSuccess)
+        return cuda_fail(e, "upload of H");
+    if (T && (e = cudaMemcpyAsync(T, temperatures_host, ub * 4, cudaMemcpyDefault, up)) !=
                  cudaSuccess)
         return cuda_fail(e, "upload of the temperatures");
-    if ((st = fs_sample_ex(H, W, B, V, D, temperature, T, seed, offset, 0, idx, score, nullptr,
-                           ws, p.wsBytes, stream)) != FS_OK)
+    if (overlap) {
+        if ((e = cudaEventRecord(h.uploaded[j], up)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(s, h.uploaded[j], 0)) != cudaSuccess)
+            return cuda_fail(e, "upload ordering");
+    }
+    if ((st = fs_sample_ex(H, W, B, V, D, temperature, T, seed, offset, 0, idx_dev, score_dev,
+                           nullptr, ws, p.wsBytes, stream)) != FS_OK)
         return st;
-    if ((e = cudaMemcpyAsync(out_idx_host, idx, ub * 8, cudaMemcpyDefault, s)) != cudaSuccess)
+    if (overlap && (e = cudaEventRecord(h.consumed[j], s)) != cudaSuccess)
+        return cuda_fail(e, "slot release");
+    if (stage_idx &&
+        (e = cudaMemcpyAsync(out_idx_host, idx_dev, ub * 8, cudaMemcpyDefault, s)) != cudaSuccess)
         return cuda_fail(e, "read-back of out_idx");
-    if (score && (e = cudaMemcpyAsync(out_score_host, score, ub * 4, cudaMemcpyDefault, s)) !=
-                     cudaSuccess)
+    if (stage_score && (e = cudaMemcpyAsync(out_score_host, score_dev, ub * 4,
+                                            cudaMemcpyDefault, s)) != cudaSuccess)
         return cuda_fail(e, "read-back of out_score");
     return FS_OK;
 }
@@ -751,6 +837,21 @@ fs_status fs_release_workspaces(void) {
         if (e != cudaSuccess && st == FS_OK) st = cuda_fail(e, "cudaFree(workspace)");
     }
     g_ws.clear();
+    std::lock_guard<std::mutex> lock2(g_host_mu);
+    for (auto &kv : g_host) {
+        HostPath &h = kv.second;
+        cudaSetDevice(kv.first.first);
+        if (h.block) {
+            cudaError_t e = cudaFree(h.block);
+            if (e != cudaSuccess && st == FS_OK) st = cuda_fail(e, "cudaFree(host-path staging)");
+        }
+        for (int j = 0; j < 2; ++j) {
+            if (h.uploaded[j]) cudaEventDestroy(h.uploaded[j]);
+            if (h.consumed[j]) cudaEventDestroy(h.consumed[j]);
+        }
+        if (h.copy) cudaStreamDestroy(h.copy);
+    }
+    g_host.clear();
     cudaSetDevice(cur);
     return st;
 }

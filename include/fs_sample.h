@@ -107,22 +107,28 @@ fs_status fs_sample(const void *H, const void *W, int64_t B, int64_t V, int64_t 
  * fs_sample_host -- fs_sample with the per-call data in HOST memory, for a
  * decode loop whose hidden states and sampled tokens live on the host.  The
  * weights stay resident on the device (method section: W is read from HBM
- * once per call).  On `stream`, in order: copy H (and the temperatures) to the
- * device, Stage 1, Stage 2, copy the indices (and scores) back.
- *   H_host            host bf16 [B, D], row-major; page-locked memory makes
- *                     the upload asynchronous (pageable memory is staged by
- *                     the CUDA runtime before the call returns)
+ * once per call).
+ *   H_host            host bf16 [B, D], row-major; must stay unchanged until
+ *                     `stream` reaches the end of the call
  *   W                 device bf16 [V, D], row-major, 16-byte aligned
- *   temperatures_host NULL or host f32 [B]
- *   out_idx_host      host int64 [B]; valid once the stream has reached the
- *                     end of this call (cudaStreamSynchronize or an event).
- *                     With pageable memory the read-back completes before
- *                     the call returns.
+ *   temperatures_host NULL or host f32 [B] (same lifetime rule as H_host)
+ *   out_idx_host      host int64 [B]; valid once `stream` has reached the end
+ *                     of this call (cudaStreamSynchronize or an event)
  *   out_score_host    NULL or host f32 [B], as out_idx_host
- * The device copies of H, the temperatures and the outputs live in the same
- * per-(device, stream) cached block as fs_sample's workspace; calls on one
- * stream reuse it in order.  Host pointers need no particular alignment.
- * Results are bit-identical to fs_sample on the same data.
+ * Order of work: H (and the temperatures) are copied into one of two device
+ * slots used alternately, on an internal upload stream that waits for the
+ * previous reader of that slot, so that the upload overlaps the previous
+ * call's kernels; `stream` waits for the upload, then runs Stage 1 and
+ * Stage 2.  Page-locked outputs are written by Stage 2 directly through their
+ * mapped device address; pageable outputs are staged on the device and copied
+ * back on `stream` (that copy completes before the call returns).  Page-locked
+ * inputs keep the upload asynchronous; pageable inputs are staged by the CUDA
+ * runtime.  While `stream` is being captured into a CUDA graph, the upload is
+ * issued on `stream` itself and every host buffer must be page-locked.
+ * Device state (upload stream, events, slots) is cached per (device, stream)
+ * and freed by fs_release_workspaces().  Host pointers need no particular
+ * alignment beyond their element size for page-locked outputs.  Results are
+ * bit-identical to fs_sample on the same data.
  * ------------------------------------------------------------------------- */
 fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V, int64_t D,
                          float temperature, const float *temperatures_host, uint64_t seed,

@@ -253,6 +253,36 @@ def test_host_buffer_entry(fs, dev):
     compare_indices(ti.numpy(), o_idx, o_best, o_second, "host buffers")
 
 
+def test_host_buffer_entry_growth_and_graph_capture(fs, dev):
+    """fs_sample_host grows its staging between batch sizes, and under CUDA
+    graph capture (upload on the captured stream) replays to the same draw."""
+    g = torch.Generator(device="cpu").manual_seed(44)
+    W = (torch.randn((9001, 64), generator=g) * 0.1).to(torch.bfloat16).to(dev)
+    for B in (3, 200, 3, 129):
+        H = torch.randn((B, 64), generator=g).to(torch.bfloat16)
+        ref, rs = fs.fs_sample(H.to(dev), W, temperature=0.7, seed=8, offset=B)
+        idx, sc = fs.fs_sample_host(H.pin_memory(), W, temperature=0.7, seed=8, offset=B)
+        torch.cuda.synchronize()
+        assert torch.equal(ref.cpu(), idx) and torch.equal(rs.cpu(), sc)
+    B = 40
+    H = torch.randn((B, 64), generator=g).to(torch.bfloat16).pin_memory()
+    T = (0.5 + torch.rand(B, generator=g)).pin_memory()
+    ref, rs = fs.fs_sample(H.to(dev), W, temperature=T.to(dev), seed=9, offset=4)
+    s = torch.cuda.Stream()
+    idx = torch.empty(B, dtype=torch.int64).pin_memory()
+    sc = torch.empty(B, dtype=torch.float32).pin_memory()
+    with torch.cuda.stream(s):  # warm-up: staging and workspace exist before capture
+        fs.fs_sample_host(H, W, temperature=T, seed=9, offset=4, out_idx=idx, out_score=sc)
+    s.synchronize()
+    idx.fill_(-7)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        fs.fs_sample_host(H, W, temperature=T, seed=9, offset=4, out_idx=idx, out_score=sc)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(ref.cpu(), idx) and torch.equal(rs.cpu(), sc)
+
+
 # ---------------------------------------------------------------- unfused comparator
 
 @pytest.mark.parametrize("T", [0.8, 1e-3, 0.3, 50.0, "rows"])
