@@ -71,6 +71,7 @@ SIGNATURES = {
     "fs_sample_unfused": ([_vp, _vp, _i64, _i64, _i64, _f32, _vp, _u64, _u64, _vp, _int, _vp, _vp,
                            _vp, _sz, _vp], _int),
     "fs_debug_noise": ([_u64, _u64, _i64, _i64, _i64, _vp, _vp, _vp], _int),
+    "fs_debug_gumbel": ([_vp, _i64, _vp, _vp], _int),
     "fs_get_device_status": ([_vp, ctypes.POINTER(_u32)], _int),
     "fs_plan_info": ([_i64, _i64, _i64, _int, ctypes.POINTER(_i64)], _int),
     "fs_release_workspaces": ([], _int),
@@ -402,6 +403,16 @@ def fs_debug_noise(seed, offset, b0, nb, V, device=None, stream=None):
     g = torch.empty((nb, V), dtype=torch.float32, device=dev)
     _check(lib().fs_debug_noise(seed, offset, b0, nb, V, _ptr(words), _ptr(g), _stream(stream)))
     return words, g
+
+
+def fs_debug_gumbel(words, stream=None):
+    """g f32 [n] of the device Gumbel transform applied to uint32 words (as int32) [n]."""
+    if not isinstance(words, torch.Tensor) or not words.is_cuda or words.dtype != torch.int32 \
+            or not words.is_contiguous():
+        raise FSError(FS_ERR_INVALID_ARG, "words must be a contiguous int32 CUDA tensor")
+    g = torch.empty(words.shape, dtype=torch.float32, device=words.device)
+    _check(lib().fs_debug_gumbel(_ptr(words), words.numel(), _ptr(g), _stream(stream)))
+    return g
 
 
 def fs_get_device_status(stream=None) -> int:

@@ -812,6 +812,20 @@ fs_status fs_debug_noise(uint64_t seed, uint64_t offset, int64_t b0, int64_t nb,
     return FS_OK;
 }
 
+fs_status fs_debug_gumbel(const uint32_t *words, int64_t n, float *out_g, void *stream) {
+    if (!words || !out_g || n < 1)
+        return fail(FS_ERR_INVALID_ARG, "need words, out_g and n >= 1");
+    fs_status st;
+    if ((st = validate_out(words, 4, "words")) != FS_OK) return st;
+    if ((st = validate_out(out_g, 4, "out_g")) != FS_OK) return st;
+    int dev;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    cudaError_t e = launch_debug_gumbel(words, n, out_g, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "debug gumbel launch");
+    return FS_OK;
+}
+
 fs_status fs_get_device_status(void *stream, uint32_t *out_word) {
     int dev;
     DeviceInfo info;

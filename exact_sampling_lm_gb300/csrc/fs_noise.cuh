@@ -108,19 +108,47 @@ __device__ __forceinline__ void philox4x64_10_block(uint64_t c0, uint64_t c1, ui
     w[3] = c3;
 }
 
-// u = ((x >> 8) | 1) * 2^-24: exact in f32, never 0 or 1, symmetric about 1/2.
-__device__ __forceinline__ float uniform_from_word(uint32_t x) {
-    return static_cast<float>((x >> 8) | 1u) * 0x1p-24f;
+// The uniform of a 32-bit word x is u = k * 2^-24 with k = (x >> 8) | 1: exact
+// in f32, never 0 or 1, symmetric about 1/2.
+
+// log2(x) from the hardware approximation (absolute error about 2^-22).
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-// g = -log(-log(u)) with CUDA's accurate single-precision logf (not the
-// approximate __logf, whose absolute error is fatal near u = 1 where -log(u)
-// is tiny).  The two roundings keep |g - g_exact| within a few ulp of g plus
-// about 1e-7 absolute.
+// w = -log(u) for u = k * 2^-24 (k odd, 0 < k < 2^24), within about 1 ulp.
+// For u >= 15/16 -- the only u that can still win once a row's running best
+// is established, since the screen only passes u above exp(-exp(-d)) -- the
+// Mercator series -log(1 - e) = e + e^2/2 + e^3/3 + ... in e = 1 - u, which
+// is exact in f32 here.  Six terms: the dropped tail (e^n/n for n >= 7) is
+// below e^6/7 * 1/(1-e) <= 2^-24/6 relative to w for e <= 2^-4, well under
+// half an ulp.
+// Otherwise CUDA's accurate logf.  (The approximate __logf is not usable for
+// this inner logarithm: its absolute error is fatal near u = 1, where w is
+// tiny and the Gumbel large.)
+constexpr uint32_t kSeriesMinK = 15u << 20;  // u >= 15/16
+__device__ __forceinline__ float neglog_uniform(uint32_t k) {
+    if (k >= kSeriesMinK) {
+        const float e = static_cast<float>((1u << 24) - k) * 0x1p-24f;  // exact
+        float p = fmaf(e, 1.0f / 6.0f, 0.2f);
+        p = fmaf(p, e, 0.25f);
+        p = fmaf(p, e, 1.0f / 3.0f);
+        p = fmaf(p, e, 0.5f);
+        p = fmaf(p, e, 1.0f);
+        return p * e;
+    }
+    return -logf(static_cast<float>(k) * 0x1p-24f);
+}
+
+// g = -log(w), w = -log(u) in [6e-8, 16.7], from the hardware log2: its
+// absolute error (about 2^-22 in log2) becomes about 1e-7 in g, below an
+// ulp of any score s = l~ + g with |s| >= 1 and far below the screen's
+// slack; w's own error (about 1 ulp, relative) adds another 1e-7.
 __device__ __forceinline__ float gumbel_from_word(uint32_t x) {
-    const float u = uniform_from_word(x);
-    const float e = -logf(u);
-    return -logf(e);
+    const float w = neglog_uniform((x >> 8) | 1u);
+    return -0.69314718055994531f * lg2_approx(w);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -347,6 +347,23 @@ cudaError_t launch_logits_sample(const void *Y, int y_dtype, int64_t B, int64_t 
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ debug gumbel
+__global__ void debug_gumbel_kernel(const uint32_t *__restrict__ words, int64_t n,
+                                    float *__restrict__ out_g) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        out_g[i] = gumbel_from_word(words[i]);
+}
+
+cudaError_t launch_debug_gumbel(const uint32_t *words, int64_t n, float *out_g,
+                                cudaStream_t stream) {
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    if (blocks < 1) blocks = 1;
+    debug_gumbel_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(words, n, out_g);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ debug noise
 __global__ void debug_noise_kernel(uint64_t seed, uint64_t offset, int64_t b0, int64_t nb,
                                    int64_t V, uint32_t *__restrict__ out_words,

@@ -8,29 +8,33 @@
 // chunk.  Only (score, index) candidates leave the chip, never the [B, V]
 // logits.
 //
-// GB300 design (one persistent CTA per SM, 320 threads):
-//   warp 8      TMA producer: streams H [128 x 64] and W [<=256 x 64] k-blocks
+// GB300 design (one persistent CTA per SM, 576 threads = 18 warps):
+//   warp 16     TMA producer: streams H [rows x 64] and W [<=256 x 64] k-blocks
 //               (128-byte swizzled) into a 4-stage shared-memory ring.
-//   warp 9      allocates 512 TMEM columns; one thread issues
+//   warp 17     allocates 512 TMEM columns; one thread issues
 //               tcgen05.mma (M=128, N<=256, K=16, bf16 -> f32) into one of two
 //               256-column accumulators and commits to mbarriers.
-//   warps 0-7   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//               lane quarter w % 4, column half w / 4), then per element
-//               s = l * (1/T) + g with g from Philox4x64-10, and a running
-//               per-row argmax across all tiles of the CTA.  The epilogue of
-//               tile t overlaps the MMA of tile t+1 (double-buffered TMEM).
+//   warps 0-15  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lane quarter w % 4 and column quarter w / 4 of the tile), then
+//               per element s = l * (1/T) + g with g from Philox4x64-10, and a
+//               running per-row argmax across all tiles of the CTA.  The
+//               epilogue of tile t overlaps the MMA of tile t+1 (double-buffered
+//               TMEM).  At the end the four column quarters of each row are
+//               merged through shared memory.
 // Batch rows sit on the MMA M dimension, so each epilogue thread owns one row
-// and scans the vocabulary in increasing order: the lowest-index tie rule and
-// the 8-wide Philox block both fall out without cross-thread exchange.
+// and scans its columns in increasing order: the lowest-index tie rule and
+// the 8-wide Philox block both fall out without cross-lane exchange.
 // CTA c works on batch tile c % nM and vocabulary partition c / nM
 // (partitions are balanced in 16-row units), and writes one candidate per
-// (row, partition, column half).  A partition is cut into 256-row tiles plus
-// a final 32-row tile, so that the one epilogue that cannot overlap an MMA
-// (the last) is short.  Each CTA starts its K loop at a different k-block,
-// so the CTAs do not all request the same H line from L2 at once.
+// (row, partition).  Without clusters a partition is cut into balanced tiles
+// of at most 256 rows plus a final 128-row tile, so that the one epilogue
+// that cannot overlap an MMA (the last) is short; paired CTAs use plain
+// 256-row tiles.  Each CTA (each cluster, when paired) starts its K loop at a
+// different k-block, so the CTAs do not all request the same H line from L2
+// at once.
 // The epilogue screens every element with a cheap conservative bound
-// (screen_threshold): only elements that may beat the running best pay for
-// the two accurate logarithms, and the result equals the unscreened scan.
+// (screen_kbound): only elements that may beat the running best pay for the
+// exact Gumbel, and the result equals the unscreened scan.
 //
 // Every wait is bounded: on expiry the CTA raises the device error word,
 // tells its other warps to stop, drains its own TMA loads and MMAs, frees TMEM

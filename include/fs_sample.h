@@ -298,6 +298,14 @@ fs_status fs_debug_noise(uint64_t seed, uint64_t offset, int64_t b0, int64_t nb,
                          int64_t V, uint32_t *out_words, float *out_g, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * fs_debug_gumbel -- test hook: g = -log(-log(u)) of given 32-bit random
+ * words (u = ((x >> 8) | 1) * 2^-24, see Noise above), by the device function
+ * every sampling kernel uses.
+ *   words  device uint32 [n];  out_g  device f32 [n];  both 4-byte aligned
+ * ------------------------------------------------------------------------- */
+fs_status fs_debug_gumbel(const uint32_t *words, int64_t n, float *out_g, void *stream);
+
+/* ---------------------------------------------------------------------------
  * fs_get_device_status -- synchronise `stream`, then read and clear the
  * library's device error word on the current device.  *out_word (may be
  * NULL) receives the raw bits: 1 = a bounded wait inside a kernel expired.

@@ -126,6 +126,9 @@ def test_other_entry_points_validate():
                                    16, None, 16, 1 << 20, None) == _lib.FS_ERR_INVALID_ARG
     assert L.fs_debug_noise(0, 0, -1, 1, 8, 16, None, None) == _lib.FS_ERR_INVALID_ARG
     assert L.fs_debug_noise(0, 0, 0, 1, 8, None, None, None) == _lib.FS_ERR_INVALID_ARG
+    assert L.fs_debug_gumbel(None, 8, 16, None) == _lib.FS_ERR_INVALID_ARG
+    assert L.fs_debug_gumbel(16, 0, 16, None) == _lib.FS_ERR_INVALID_ARG
+    assert L.fs_debug_gumbel(18, 8, 16, None) == _lib.FS_ERR_UNSUPPORTED
     out = (ctypes.c_int64 * 6)()
     assert L.fs_plan_info(4, 64, 64, 0, out) == _lib.FS_ERR_INVALID_ARG
     assert L.fs_workspace_size(0, 64, 64) == 0

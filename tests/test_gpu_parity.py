@@ -112,6 +112,28 @@ def test_noise_words_bit_exact_and_gumbel_within_bound(fs, dev):
             nb, V, err.max(), float((err / ulp).max())))
 
 
+def test_gumbel_transform_exhaustive(fs, dev):
+    """Every one of the 2^23 distinct uniforms u = k 2^-24 (k odd): the device
+    Gumbel is within 2 ulp(g) + 3e-7 of the oracle's (double, rounded once).
+    That bound covers w = -log u to about 1 ulp and the hardware log2's
+    absolute error of about 2^-22 in the outer logarithm."""
+    k = np.arange(1, 1 << 24, 2, dtype=np.uint32)
+    words = (k << np.uint32(8)).view(np.int32)
+    g = fs.fs_debug_gumbel(torch.from_numpy(words).to(dev))
+    torch.cuda.synchronize()
+    gg = g.cpu().numpy().astype(np.float64)
+    og = oracle.gumbel_block(words.view(np.uint32)).astype(np.float64)
+    ulp = np.spacing(np.abs(og).astype(np.float32)).astype(np.float64)
+    err = np.abs(gg - og)
+    bad = err > 2 * ulp + 3e-7
+    assert not bad.any(), "%d uniforms out of bound, first k = %d (err %g)" % (
+        int(bad.sum()), int(k[bad][0]), float(err[bad][0]))
+    # the series branch (u >= 15/16) holds the large Gumbels that win
+    hi = k >= (15 << 20)
+    print("gumbel: max |dg| = %.3e overall, %.3e for u >= 15/16; max in ulps %.2f" % (
+        err.max(), err[hi].max(), float((err / ulp).max())))
+
+
 # ---------------------------------------------------------------- small exhaustive cases
 
 def test_tiny_workload(fs, dev):
