@@ -313,10 +313,28 @@ struct CachedWs {
 static std::mutex g_ws_mu;
 static std::map<std::pair<int, void *>, CachedWs> g_ws;
 
+// True while `stream` is being captured into a CUDA graph.  Device memory
+// allocated then would belong to the graph, so the caches below never grow
+// during a capture.
+static bool stream_capturing(cudaStream_t stream) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return cap != cudaStreamCaptureStatusNone;
+}
+
 static fs_status cached_workspace(int dev, cudaStream_t stream, size_t need, void **out) {
     std::lock_guard<std::mutex> lock(g_ws_mu);
     CachedWs &c = g_ws[std::make_pair(dev, static_cast<void *>(stream))];
     if (c.bytes < need) {
+        if (stream_capturing(stream))
+            return fail(FS_ERR_UNSUPPORTED,
+                        "the cached workspace of this stream (%zu bytes) cannot grow to %zu "
+                        "during stream capture: make one call of the same size on this stream "
+                        "before capturing, or pass a workspace to fs_sample_ex",
+                        c.bytes, need);
         size_t grow = 65536;
         while (grow < need) grow <<= 1;
         if (c.ptr) {
@@ -481,8 +499,12 @@ struct HostPath {
 static std::mutex g_host_mu;
 static std::map<std::pair<int, void *>, HostPath> g_host;
 
-static fs_status host_path_ready(HostPath &h, size_t need) {
+static fs_status host_path_ready(HostPath &h, size_t need, bool capturing) {
     cudaError_t e;
+    if (capturing && (!h.copy || h.bytes < need))
+        return fail(FS_ERR_UNSUPPORTED,
+                    "fs_sample_host cannot set up or grow its device staging during stream "
+                    "capture: make one call of the same size on this stream before capturing");
     if (!h.copy) {
         if ((e = cudaStreamCreateWithFlags(&h.copy, cudaStreamNonBlocking)) != cudaSuccess)
             return cuda_fail(e, "cudaStreamCreate(upload stream)");
@@ -548,17 +570,15 @@ fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V
     const size_t i_b = round256(ub * 8);
     const size_t s_b = round256(ub * 4);
 
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    cudaError_t e = cudaStreamIsCapturing(s, &cap);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
     // Under stream capture the upload stays on the caller's stream (a graph
     // cannot wait on events recorded outside it); otherwise it runs on the
     // internal upload stream and overlaps the previous call's kernels.
-    const bool overlap = cap == cudaStreamCaptureStatusNone;
+    const bool overlap = !stream_capturing(s);
 
     std::lock_guard<std::mutex> lock(g_host_mu);
     HostPath &h = g_host[std::make_pair(dev, static_cast<void *>(s))];
-    if ((st = host_path_ready(h, 2 * (h_b + t_b) + i_b + s_b)) != FS_OK) return st;
+    if ((st = host_path_ready(h, 2 * (h_b + t_b) + i_b + s_b, !overlap)) != FS_OK) return st;
+    cudaError_t e;
     const int j = h.next;
     h.next ^= 1;
     char *slot = h.block + j * (h_b + t_b);

@@ -97,7 +97,11 @@ typedef enum fs_status {
  * Candidate workspace: a buffer cached per (device, stream) inside the
  * library, grown stream-ordered with cudaMallocAsync/cudaFreeAsync.  Calls on
  * one stream reuse it in order.  fs_release_workspaces() frees the cache.
- * Returns FS_ERR_NO_MEMORY if the workspace cannot be grown.
+ * Returns FS_ERR_NO_MEMORY if the workspace cannot be grown.  While `stream`
+ * is being captured into a CUDA graph the cache does not grow (memory
+ * allocated then would belong to the graph): a call that needs more than an
+ * earlier call of the same stream left returns FS_ERR_UNSUPPORTED; make one
+ * call of the same size before capturing, or use fs_sample_ex.
  * ------------------------------------------------------------------------- */
 fs_status fs_sample(const void *H, const void *W, int64_t B, int64_t V, int64_t D,
                     float temperature, const float *temperatures, uint64_t seed,
@@ -124,7 +128,9 @@ fs_status fs_sample(const void *H, const void *W, int64_t B, int64_t V, int64_t 
  * back on `stream` (that copy completes before the call returns).  Page-locked
  * inputs keep the upload asynchronous; pageable inputs are staged by the CUDA
  * runtime.  While `stream` is being captured into a CUDA graph, the upload is
- * issued on `stream` itself and every host buffer must be page-locked.
+ * issued on `stream` itself, every host buffer must be page-locked, and the
+ * device staging must already exist from an earlier call of the same size
+ * on that stream (else FS_ERR_UNSUPPORTED, as for fs_sample).
  * Device state (upload stream, events, slots) is cached per (device, stream)
  * and freed by fs_release_workspaces().  Host pointers need no particular
  * alignment beyond their element size for page-locked outputs.  Results are

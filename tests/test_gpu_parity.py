@@ -305,6 +305,42 @@ def test_host_buffer_entry_growth_and_graph_capture(fs, dev):
     assert torch.equal(ref.cpu(), idx) and torch.equal(rs.cpu(), sc)
 
 
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
+def test_graph_capture_of_fs_sample(fs, dev):
+    """fs_sample captured into a CUDA graph after one call on the capture stream
+    replays to the direct call's draw; on a fresh stream, capture refuses to
+    grow the cached workspace (graph-owned memory must not enter the cache)."""
+    g = torch.Generator(device="cpu").manual_seed(45)
+    B, V, D = 24, 12011, 128
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.1).to(torch.bfloat16).to(dev)
+    ref, rs = fs.fs_sample(H, W, temperature=0.9, seed=11, offset=3)
+    s = torch.cuda.Stream()
+    idx = torch.empty(B, dtype=torch.int64, device=dev)
+    sc = torch.empty(B, dtype=torch.float32, device=dev)
+    with torch.cuda.stream(s):
+        fs.fs_sample(H, W, temperature=0.9, seed=11, offset=3, out_idx=idx, out_score=sc)
+    s.synchronize()
+    idx.fill_(-7)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        fs.fs_sample(H, W, temperature=0.9, seed=11, offset=3, out_idx=idx, out_score=sc)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(ref, idx) and torch.equal(rs, sc)
+    H_h = H.cpu().pin_memory()
+    idx_h = torch.empty(B, dtype=torch.int64).pin_memory()
+    fresh = torch.cuda.Stream()
+    empty = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(empty, stream=fresh):
+        with pytest.raises(fs.FSError, match="capture"):
+            fs.fs_sample(H, W, temperature=0.9, seed=11, offset=3, out_idx=idx)
+        with pytest.raises(fs.FSError, match="capture"):
+            fs.fs_sample_host(H_h, W, temperature=0.9, seed=11, offset=3, out_idx=idx_h,
+                              want_score=False)
+    torch.cuda.synchronize()
+
+
 # ---------------------------------------------------------------- unfused comparator
 
 @pytest.mark.parametrize("T", [0.8, 1e-3, 0.3, 50.0, "rows"])
