@@ -165,9 +165,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // and the factor (1 - 2^-12) absorbs the relative error of the two nested
 // hardware exp2 approximations (about e1 * 1.8e-6 + 2.4e-7 for e1 =
 // exp(slack - d); below 2^-12 for every e1 <= 133, and for larger e1 the
-// true threshold is under 2^-190, far below the smallest u = 2^-24).  Elements with u <= threshold cannot win and
-// skip the two accurate logarithms; the others take the exact path, so the
-// result equals the unscreened scan.  Non-finite cases: best = -inf gives 0
+// true threshold is under 2^-190, far below the smallest u = 2^-24).  The
+// computed g (gumbel_from_word) is within a few 1e-6 of the true Gumbel, far
+// inside the slack.  Elements with u <= threshold cannot win and skip
+// gumbel_from_word; the others take the exact path, so the result equals the
+// unscreened scan.  Non-finite cases: best = -inf gives 0
 // (always exact path); NaN d gives NaN (comparison false: such an element
 // cannot win either).
 constexpr float kScreenSlack = 0x1p-10f;
