@@ -341,6 +341,50 @@ def test_graph_capture_of_fs_sample(fs, dev):
     torch.cuda.synchronize()
 
 
+def test_concurrent_host_threads(fs, dev):
+    """Two host threads, each with its own stream, call fs_sample and
+    fs_sample_host at the same time (ctypes releases the GIL): the library's
+    caches are per (device, stream) and locked, so every result equals the
+    sequential one."""
+    import threading
+    g = torch.Generator(device="cpu").manual_seed(46)
+    B, V, D = 40, 20011, 128
+    W = (torch.randn((V, D), generator=g) * 0.1).to(torch.bfloat16).to(dev)
+    Hs = [torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev) for _ in range(2)]
+    refs = [[fs.fs_sample(Hs[t], W, temperature=0.8, seed=t, offset=k)[0] for k in range(20)]
+            for t in range(2)]
+    torch.cuda.synchronize()
+    outs = [[None] * 20 for _ in range(2)]
+    errors = []
+
+    def worker(t):
+        try:
+            torch.cuda.set_device(dev)
+            s = torch.cuda.Stream()
+            H_h = Hs[t].cpu().pin_memory()
+            with torch.cuda.stream(s):
+                for k in range(20):
+                    if k % 2:
+                        outs[t][k] = fs.fs_sample_host(H_h, W, temperature=0.8, seed=t,
+                                                       offset=k, want_score=False)[0]
+                    else:
+                        outs[t][k] = fs.fs_sample(Hs[t], W, temperature=0.8, seed=t,
+                                                  offset=k)[0]
+            s.synchronize()
+        except Exception as e:  # reported in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for t in range(2):
+        for k in range(20):
+            assert torch.equal(refs[t][k].cpu(), outs[t][k].cpu()), (t, k)
+
+
 # ---------------------------------------------------------------- unfused comparator
 
 @pytest.mark.parametrize("T", [0.8, 1e-3, 0.3, 50.0, "rows"])
