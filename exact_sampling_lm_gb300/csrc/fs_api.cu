@@ -261,15 +261,18 @@ static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &
                             uint64_t offset, uint32_t flags, float *out_logits, void *out_y,
                             int y_dtype, const Candidates *cand, cudaStream_t stream,
                             const fs_transforms *tf = nullptr, int64_t vocab_offset = 0) {
-    CUtensorMap tmH, tmW64, tmW16;
+    CUtensorMap tmH;
+    WMaps wm;
     fs_status st;
     // With one batch tile, load only the live rows of H (rounded up to the
     // 8-row swizzle atom); the MMA's other A rows feed TMEM lanes that the
     // epilogue never reads.
     const int h_box_rows = p.nM == 1 ? static_cast<int>((p.B + 7) / 8 * 8) : kBM;
     if ((st = make_tmap(&tmH, H, p.B, p.D, static_cast<uint32_t>(h_box_rows))) != FS_OK) return st;
-    if ((st = make_tmap(&tmW64, W, p.V, p.D, 64)) != FS_OK) return st;
-    if ((st = make_tmap(&tmW16, W, p.V, p.D, 16)) != FS_OK) return st;
+    if ((st = make_tmap(&wm.w16, W, p.V, p.D, 16)) != FS_OK) return st;
+    if ((st = make_tmap(&wm.w64, W, p.V, p.D, 64)) != FS_OK) return st;
+    if ((st = make_tmap(&wm.w128, W, p.V, p.D, 128)) != FS_OK) return st;
+    if ((st = make_tmap(&wm.w256, W, p.V, p.D, 256)) != FS_OK) return st;
     Stage1Args a;
     a.B = static_cast<int32_t>(p.B);
     a.V = static_cast<int32_t>(p.V);
@@ -300,7 +303,7 @@ static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &
     a.allow_mask = tf ? tf->allow_mask : nullptr;
     a.mask_words = tf ? tf->mask_words : 0;
     a.timeout_ns = wait_timeout_ns();
-    cudaError_t e = launch_stage1(mode, tmH, tmW64, tmW16, a, p.G, stream);
+    cudaError_t e = launch_stage1(mode, tmH, wm, a, p.G, stream);
     if (e != cudaSuccess) return cuda_fail(e, "Stage 1 launch");
     return FS_OK;
 }

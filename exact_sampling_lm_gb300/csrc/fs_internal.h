@@ -85,8 +85,15 @@ struct Stage1Args {
     uint64_t timeout_ns;
 };
 
-cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const CUtensorMap &tmW64,
-                          const CUtensorMap &tmW16, const Stage1Args &a, int grid,
+// W is read through four tensor maps with boxes of 16, 64, 128 and 256 rows
+// (all 64 columns wide): whole tiles in one box per CTA, tails in 64- and
+// 16-row boxes.
+struct WMaps {
+    CUtensorMap w16, w64, w128, w256;
+};
+
+cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const WMaps &wm,
+                          const Stage1Args &a, int grid,
                           cudaStream_t stream);
 
 cudaError_t launch_stage2(const float *cand_score, const int32_t *cand_idx, int nCand,

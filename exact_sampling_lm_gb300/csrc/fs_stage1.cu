@@ -10,10 +10,15 @@
 //
 // GB300 design (one persistent CTA per SM, 576 threads = 18 warps):
 //   warp 16     TMA producer: streams H [rows x 64] and W [<=256 x 64] k-blocks
-//               (128-byte swizzled) into a 4-stage shared-memory ring.
+//               (128-byte swizzled) into a 4-stage shared-memory ring; a whole
+//               W tile is one 256-row box (one 128-row box per CTA when
+//               paired), tails are 64- and 16-row boxes.
 //   warp 17     allocates 512 TMEM columns; one thread issues
 //               tcgen05.mma (M=128, N<=256, K=16, bf16 -> f32) into one of two
 //               256-column accumulators and commits to mbarriers.
+//   The producer and the MMA issuer share SM sub-partitions 0 and 1 with
+//   busy epilogue warps, so they issue as few instructions per k-block as
+//   possible (whole-tile boxes, precomputed descriptors).
 //   warps 0-15  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
 //               lane quarter w % 4 and column quarter w / 4 of the tile), then
 //               per element s = l * (1/T) + g with g from Philox4x64-10, and a
@@ -266,8 +271,10 @@ __device__ __forceinline__ void store_bf16_chunk(__nv_bfloat16 *dst, int n,
 // MMAs have released it (their commits arrive on both CTAs' empty barriers).
 template <int MODE, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
-    stage1_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW64,
-                  const __grid_constant__ CUtensorMap tmW16, const Stage1Args a) {
+    stage1_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW16,
+                  const __grid_constant__ CUtensorMap tmW64,
+                  const __grid_constant__ CUtensorMap tmWhalf,
+                  const __grid_constant__ CUtensorMap tmWfull, const Stage1Args a) {
     constexpr bool kSample = (MODE == kModeSample || MODE == kModeSampleStore ||
                               MODE == kModeSampleLogprob || MODE == kModeSampleXform ||
                               MODE == kModeSampleXformLogprob);
@@ -341,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmH);
             prefetch_tmap(&tmW64);
             prefetch_tmap(&tmW16);
+            prefetch_tmap(CS > 1 ? &tmWhalf : &tmWfull);
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_h = l2_policy_evict_last();
             const uint32_t h_bytes = static_cast<uint32_t>(a.h_box_rows) * (kBK * 2);
@@ -370,7 +378,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *dB = sB + stage * kBBytes;
                     const int kx = kb * kBK;
                     tma_load_2d(dA, &tmH, &full_bar[stage], kx, m * kBM, pol_h);
-                    if (CS == 1) {
+                    if (tn16 == kBN) {
+                        // a whole tile: one box per CTA (half of it each, multicast, when
+                        // paired); same shared-memory layout as the 64-row boxes
+                        if (CS == 1)
+                            tma_load_2d(dB, &tmWfull, &full_bar[stage], kx, v0, pol_w);
+                        else
+                            tma_load_2d_multicast(dB + crank * (kBN / 2) * (kBK * 2), &tmWhalf,
+                                                  &full_bar[stage], kx,
+                                                  v0 + static_cast<int>(crank) * (kBN / 2),
+                                                  kClusterMask, pol_w);
+                    } else if (CS == 1) {
                         for (int i = 0; i < n64; ++i)
                             tma_load_2d(dB + i * 64 * (kBK * 2), &tmW64, &full_bar[stage], kx,
                                         v0 + i * 64, pol_w);
@@ -414,6 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(sA));
+            const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(sB));
             for (int t = 0; t < ntiles && ok; ++t) {
                 const int acc = t & 1;
                 const uint32_t aphase = static_cast<uint32_t>(t >> 1) & 1u;
@@ -432,13 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a_addr = smem_u32(sA + stage * kABytes);
-                    const uint32_t b_addr = smem_u32(sB + stage * kBBytes);
+                    {
+                        // descriptors differ from stage 0's by the stage offset and
+                        // from each other by 32 bytes of K (both in 16-byte units)
+                        const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage * (kABytes >> 4));
+                        const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (kBBytes >> 4));
 #pragma unroll
-                    for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
-                        umma_bf16_ss(d_tmem, sw128_kmajor_desc(a_addr + ks * kUmmaK * 2),
-                                     sw128_kmajor_desc(b_addr + ks * kUmmaK * 2), idesc,
-                                     (j | ks) != 0 ? 1u : 0u);
+                        for (int ks = 0; ks < kBK / kUmmaK; ++ks)
+                            umma_bf16_ss(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc,
+                                         (j | ks) != 0 ? 1u : 0u);
                     }
                     if (CS > 1)
                         umma_commit_multicast(&empty_bar[stage], kClusterMask);
@@ -677,8 +699,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int MODE, int CS>
-static cudaError_t launch_mode(const CUtensorMap &tmH, const CUtensorMap &tmW64,
-                               const CUtensorMap &tmW16, const Stage1Args &a, int grid,
+static cudaError_t launch_mode(const CUtensorMap &tmH, const WMaps &wm, const Stage1Args &a,
+                               int grid,
                                cudaStream_t stream) {
     static std::atomic<uint32_t> configured_mask{0};  // per device (device ordinals < 32)
     int dev = 0;
@@ -707,7 +729,8 @@ static cudaError_t launch_mode(const CUtensorMap &tmH, const CUtensorMap &tmW64,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, stage1_kernel<MODE, CS>, tmH, tmW64, tmW16, a);
+    return cudaLaunchKernelEx(&cfg, stage1_kernel<MODE, CS>, tmH, wm.w16, wm.w64, wm.w128,
+                              wm.w256, a);
 }
 
 // How many 2-CTA clusters of Stage 1 the current device can hold at once
@@ -746,40 +769,40 @@ static int max_pair_clusters() {
     return cached[dev];
 }
 
-cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const CUtensorMap &tmW64,
-                          const CUtensorMap &tmW16, const Stage1Args &a, int grid,
+cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const WMaps &wm,
+                          const Stage1Args &a, int grid,
                           cudaStream_t stream) {
     // Pairs only when batch tiles come in pairs and every pair fits at once.
     const bool pair = (a.nM % 2 == 0) && (2 * max_pair_clusters() >= grid);
     if (pair) {
         switch (mode) {
-            case kModeSample: return launch_mode<kModeSample, 2>(tmH, tmW64, tmW16, a, grid, stream);
+            case kModeSample: return launch_mode<kModeSample, 2>(tmH, wm, a, grid, stream);
             case kModeSampleStore:
-                return launch_mode<kModeSampleStore, 2>(tmH, tmW64, tmW16, a, grid, stream);
+                return launch_mode<kModeSampleStore, 2>(tmH, wm, a, grid, stream);
             case kModeGemmBf16:
-                return launch_mode<kModeGemmBf16, 2>(tmH, tmW64, tmW16, a, grid, stream);
-            case kModeGemmF32: return launch_mode<kModeGemmF32, 2>(tmH, tmW64, tmW16, a, grid, stream);
+                return launch_mode<kModeGemmBf16, 2>(tmH, wm, a, grid, stream);
+            case kModeGemmF32: return launch_mode<kModeGemmF32, 2>(tmH, wm, a, grid, stream);
             case kModeSampleLogprob:
-                return launch_mode<kModeSampleLogprob, 2>(tmH, tmW64, tmW16, a, grid, stream);
+                return launch_mode<kModeSampleLogprob, 2>(tmH, wm, a, grid, stream);
             case kModeSampleXform:
-                return launch_mode<kModeSampleXform, 2>(tmH, tmW64, tmW16, a, grid, stream);
+                return launch_mode<kModeSampleXform, 2>(tmH, wm, a, grid, stream);
             case kModeSampleXformLogprob:
-                return launch_mode<kModeSampleXformLogprob, 2>(tmH, tmW64, tmW16, a, grid, stream);
+                return launch_mode<kModeSampleXformLogprob, 2>(tmH, wm, a, grid, stream);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (mode) {
-        case kModeSample: return launch_mode<kModeSample, 1>(tmH, tmW64, tmW16, a, grid, stream);
+        case kModeSample: return launch_mode<kModeSample, 1>(tmH, wm, a, grid, stream);
         case kModeSampleStore:
-            return launch_mode<kModeSampleStore, 1>(tmH, tmW64, tmW16, a, grid, stream);
-        case kModeGemmBf16: return launch_mode<kModeGemmBf16, 1>(tmH, tmW64, tmW16, a, grid, stream);
-        case kModeGemmF32: return launch_mode<kModeGemmF32, 1>(tmH, tmW64, tmW16, a, grid, stream);
+            return launch_mode<kModeSampleStore, 1>(tmH, wm, a, grid, stream);
+        case kModeGemmBf16: return launch_mode<kModeGemmBf16, 1>(tmH, wm, a, grid, stream);
+        case kModeGemmF32: return launch_mode<kModeGemmF32, 1>(tmH, wm, a, grid, stream);
         case kModeSampleLogprob:
-            return launch_mode<kModeSampleLogprob, 1>(tmH, tmW64, tmW16, a, grid, stream);
+            return launch_mode<kModeSampleLogprob, 1>(tmH, wm, a, grid, stream);
         case kModeSampleXform:
-            return launch_mode<kModeSampleXform, 1>(tmH, tmW64, tmW16, a, grid, stream);
+            return launch_mode<kModeSampleXform, 1>(tmH, wm, a, grid, stream);
         case kModeSampleXformLogprob:
-            return launch_mode<kModeSampleXformLogprob, 1>(tmH, tmW64, tmW16, a, grid, stream);
+            return launch_mode<kModeSampleXformLogprob, 1>(tmH, wm, a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
