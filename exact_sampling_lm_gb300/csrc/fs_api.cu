@@ -492,6 +492,7 @@ static void *mapped_host_alias(void *p) {
 // upload after the previous reader of that slot, and output staging for
 // pageable host outputs.
 struct HostPath {
+    std::mutex mu;  // serialises calls on this (device, stream)
     cudaStream_t copy = nullptr;
     cudaEvent_t uploaded[2] = {nullptr, nullptr};
     cudaEvent_t consumed[2] = {nullptr, nullptr};
@@ -578,8 +579,14 @@ fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V
     // internal upload stream and overlaps the previous call's kernels.
     const bool overlap = !stream_capturing(s);
 
-    std::lock_guard<std::mutex> lock(g_host_mu);
-    HostPath &h = g_host[std::make_pair(dev, static_cast<void *>(s))];
+    HostPath *hp;
+    {
+        // std::map never moves its nodes: the entry outlives this lookup.
+        std::lock_guard<std::mutex> map_lock(g_host_mu);
+        hp = &g_host[std::make_pair(dev, static_cast<void *>(s))];
+    }
+    HostPath &h = *hp;
+    std::lock_guard<std::mutex> lock(h.mu);
     if ((st = host_path_ready(h, 2 * (h_b + t_b) + i_b + s_b, !overlap)) != FS_OK) return st;
     cudaError_t e;
     const int j = h.next;

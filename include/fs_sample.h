@@ -353,8 +353,11 @@ fs_status fs_sample_noalloc(const void *H, const void *W, int64_t B, int64_t V, 
                             uint64_t offset, int64_t *out_idx, float *out_score,
                             void *stream);
 
-/* Frees every workspace cached by fs_sample (all devices and streams).  The
- * caller must make sure no fs_sample call is still running on the GPU. */
+/* Frees every workspace cached by fs_sample and every staging block, upload
+ * stream and event cached by fs_sample_host (all devices and streams).  It
+ * synchronises the device (cudaFree).  The caller must make sure that no
+ * other library call runs concurrently on another host thread, and that no
+ * work of those calls still needs the freed memory. */
 fs_status fs_release_workspaces(void);
 
 /* Thread-local text for the last non-FS_OK status of this thread. */
