@@ -245,6 +245,19 @@ __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]
         : "memory");
 }
 
+// Store 16 consecutive 32-bit TMEM columns of this thread's lane (the shape
+// and lane-quarter rule of tmem_ld16_wait) and wait for the store to complete.
+__device__ __forceinline__ void tmem_st16_wait(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
 // Programmatic dependent launch: allow the next kernel in the stream (launched
 // with the programmatic-serialization attribute) to be scheduled now; it still
 // waits for this grid's completion in griddep_wait().

@@ -506,6 +506,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < (warp_has_rows ? ntiles : 0); ++t) {
             const int acc = t & 1;
             const uint32_t aphase = static_cast<uint32_t>(t >> 1) & 1u;
+            // The last tile's epilogue is the one no MMA hides.  Its noise
+            // depends only on (row, column), so it is computed while that
+            // tile's MMA still runs and parked in the other accumulator:
+            // tile t-1 has released it (all epilogue warps arrived on its
+            // empty barrier) and no later MMA writes it again.
+            const bool pre_noise = kSample && !no_noise && t >= 1 && t == ntiles - 1;  // warp-uniform
+            if (pre_noise) {
+                if (!mbar_wait_bounded_backoff(&tempty_bar[acc ^ 1],
+                                               static_cast<uint32_t>((t - 1) >> 1) & 1u,
+                                               a.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                int v0p, tnp;
+                tile_geom(geom, t, v0p, tnp);
+                const int lo = col_part_start(j, tnp);
+                const int hi = col_part_start(j + 1, tnp);
+                for (int c0 = lo; c0 < hi; c0 += 16) {
+                    uint32_t wa[8], wb[8], w[16];
+                    const uint64_t v8 = static_cast<uint64_t>(a.vocab_offset + v0p + c0) >> 3;
+                    noise_words8(prow, v8, wa);
+                    noise_words8(prow, v8 + 1, wb);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        w[i] = wa[i];
+                        w[8 + i] = wb[i];
+                    }
+                    tmem_st16_wait(tmem_base + static_cast<uint32_t>((acc ^ 1) * kBN + c0) +
+                                       (static_cast<uint32_t>(q * 32) << 16),
+                                   w);
+                }
+            }
             if (!mbar_wait_bounded_backoff(&tfull_bar[acc], aphase, a.timeout_ns, abort_flag)) {
                 ok = false;
                 break;
@@ -521,6 +554,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld16_wait(tmem_base + static_cast<uint32_t>(acc * kBN + c0) +
                                        (static_cast<uint32_t>(q * 32) << 16),
                                    r);
+                    // the parked noise of the last tile, read by the whole (converged) warp
+                    uint32_t xa[8], xb[8];
+                    if (pre_noise) {
+                        uint32_t w[16];
+                        tmem_ld16_wait(tmem_base + static_cast<uint32_t>((acc ^ 1) * kBN + c0) +
+                                           (static_cast<uint32_t>(q * 32) << 16),
+                                       w);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            xa[i] = w[i];
+                            xb[i] = w[8 + i];
+                        }
+                    }
                     const int n_valid = min(16, c_hi - c0);
                     const int vbase = v0 + c0;
                     // warp-wide vote while the warp is converged; lanes without
@@ -547,10 +593,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             } else {
                                 // Both Philox blocks of the chunk first (two
                                 // independent chains for the scheduler).
-                                uint32_t xa[8], xb[8];
-                                const uint64_t v8 = static_cast<uint64_t>(a.vocab_offset + vbase) >> 3;
-                                noise_words8(prow, v8, xa);
-                                if (n_valid > 8) noise_words8(prow, v8 + 1, xb);
+                                if (!pre_noise) {
+                                    const uint64_t v8 =
+                                        static_cast<uint64_t>(a.vocab_offset + vbase) >> 3;
+                                    noise_words8(prow, v8, xa);
+                                    if (n_valid > 8) noise_words8(prow, v8 + 1, xb);
+                                }
                                 float lt[16];
                                 float lmax_a = -INFINITY, lmax_b = -INFINITY;
 #pragma unroll
