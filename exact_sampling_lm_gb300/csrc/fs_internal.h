@@ -27,7 +27,13 @@ constexpr int kWarpMma = kNumEpiWarps + 1;        // warp 17
 constexpr int kThreads = (kNumEpiWarps + 2) * 32; // 576
 constexpr int kTmemCols = 512;  // two 256-column accumulators
 constexpr int kCombineBytes = kColParts * kBM * 20;  // per-row results of the column parts
-constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 1024 + 256 + kCombineBytes;
+// Dynamic shared memory: the per-CTA maximum.  The ring takes what the
+// alignment slack, the barriers and the combine area leave: 4 stages for a
+// full batch tile, and more when a small batch shrinks each stage's H slot.
+constexpr int kSmemBytes = 232448;
+constexpr int kRingBytes = kSmemBytes - 1024 - 256 - kCombineBytes;
+constexpr int kMaxStages = 8;
+static_assert(kStages * (kABytes + kBBytes) <= kRingBytes, "ring of full batch tiles");
 constexpr int kFinalTileUnits = 8;  // last tile of a partition: 128 rows
 constexpr int kUnitRows = 16;  // vocabulary partitions are multiples of 16 rows
 

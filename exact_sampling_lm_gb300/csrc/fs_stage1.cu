@@ -285,12 +285,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    // Ring layout: nst H slots of a_stride bytes, then nst W slots.  A single
+    // batch tile loads only round_up(B, 8) rows of H per stage, so its H slot
+    // shrinks to that (in 1 KB swizzle atoms) and the ring holds more stages
+    // of W: 6 at B <= 16, 5 at B <= 88, else 4.  The MMA still reads 128 rows
+    // of A from the slot's start; the rows past the batch come from the next
+    // slots, stay inside the ring and feed accumulator lanes that no epilogue
+    // warp reads.
+    const int a_stride = (a.nM == 1) ? (a.h_box_rows * (kBK * 2) + 1023) & ~1023 : kABytes;
+    const int nst = min(kMaxStages, kRingBytes / (a_stride + kBBytes));
     uint8_t *sA = smem;
-    uint8_t *sB = smem + kStages * kABytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + kStages * kBBytes);
+    uint8_t *sB = smem + nst * a_stride;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes);
     uint64_t *full_bar = bars;
-    uint64_t *empty_bar = bars + kStages;
-    uint64_t *tfull_bar = bars + 2 * kStages;
+    uint64_t *empty_bar = bars + kMaxStages;
+    uint64_t *tfull_bar = bars + 2 * kMaxStages;
     uint64_t *tempty_bar = tfull_bar + 2;
     uint64_t *done_bar = tempty_bar + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done_bar + 1);
@@ -315,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kb_first = static_cast<int>((blockIdx.x / CS) % static_cast<unsigned>(nk));
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < nst; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], CS);
         }
@@ -374,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full_bar[stage], bytes);
-                    uint8_t *dA = sA + stage * kABytes;
+                    uint8_t *dA = sA + stage * a_stride;
                     uint8_t *dB = sB + stage * kBBytes;
                     const int kx = kb * kBK;
                     tma_load_2d(dA, &tmH, &full_bar[stage], kx, m * kBM, pol_h);
@@ -411,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     issued_mask |= 1u << stage;
                     last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kStages) {
+                    if (++stage == nst) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) raise_timeout(abort_flag);
             // Drain: every issued load must land before the CTA's shared
             // memory is released (immediate on the normal path).
-            for (int s = 0; s < kStages; ++s)
+            for (int s = 0; s < nst; ++s)
                 if (issued_mask & (1u << s))
                     mbar_wait_bounded(&full_bar[s], (last_phase_bits >> s) & 1u, a.timeout_ns,
                                       nullptr);
@@ -455,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     {
                         // descriptors differ from stage 0's by the stage offset and
                         // from each other by 32 bytes of K (both in 16-byte units)
-                        const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage * (kABytes >> 4));
+                        const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage * (a_stride >> 4));
                         const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (kBBytes >> 4));
 #pragma unroll
                         for (int ks = 0; ks < kBK / kUmmaK; ++ks)
@@ -466,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma_commit_multicast(&empty_bar[stage], kClusterMask);
                     else
                         umma_commit(&empty_bar[stage]);
-                    if (++stage == kStages) {
+                    if (++stage == nst) {
                         stage = 0;
                         phase ^= 1u;
                     }
