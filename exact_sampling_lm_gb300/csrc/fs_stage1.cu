@@ -363,8 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t h_bytes = static_cast<uint32_t>(a.h_box_rows) * (kBK * 2);
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_mask = 0;      // stages that received at least one load
-            uint32_t last_phase_bits = 0;  // phase of the last load per stage
+            int n_issued = 0;  // k-blocks whose loads were issued (for the drain)
             bool ok = true;
             // test hook (flag 0x100): issue nothing, so the consumers' first
             // bounded waits expire and the timeout path runs
@@ -418,8 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     kClusterMask, pol_w);
                         }
                     }
-                    issued_mask |= 1u << stage;
-                    last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
+                    ++n_issued;
                     if (++stage == nst) {
                         stage = 0;
                         phase ^= 1u;
@@ -430,10 +428,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) raise_timeout(abort_flag);
             // Drain: every issued load must land before the CTA's shared
             // memory is released (immediate on the normal path).
-            for (int s = 0; s < nst; ++s)
-                if (issued_mask & (1u << s))
-                    mbar_wait_bounded(&full_bar[s], (last_phase_bits >> s) & 1u, a.timeout_ns,
-                                      nullptr);
+            // The last load into stage s is load number s + nst * ((n_issued - 1 - s) / nst);
+            // its full barrier completes with parity (that number / nst) & 1.
+            for (int s = 0; s < nst && s < n_issued; ++s) {
+                const int last = s + nst * ((n_issued - 1 - s) / nst);
+                mbar_wait_bounded(&full_bar[s], static_cast<uint32_t>(last / nst) & 1u,
+                                  a.timeout_ns, nullptr);
+            }
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------ MMA issuer
