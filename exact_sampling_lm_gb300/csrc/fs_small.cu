@@ -47,7 +47,10 @@ __global__ void __launch_bounds__(kStage2Warps * 32)
     stage2_kernel(const float *__restrict__ cand_score, const int32_t *__restrict__ cand_idx,
                   int nCand, int64_t B, const float *__restrict__ temps, float temp_scalar,
                   int64_t *__restrict__ out_idx, float *__restrict__ out_score) {
-    // Launched with programmatic serialization: wait for the producing grid.
+    // The next kernel of the stream (the next call's Stage 1) may launch now:
+    // it only sets itself up before waiting for this grid.  Launched with
+    // programmatic serialization itself: wait for the producing grid.
+    griddep_launch_dependents();
     griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t b = static_cast<int64_t>(blockIdx.x) * kStage2Warps + (threadIdx.x >> 5);
@@ -115,6 +118,7 @@ __global__ void __launch_bounds__(kStage2Warps * 32)
                           float temp_scalar, int64_t *__restrict__ out_idx,
                           float *__restrict__ out_score, float *__restrict__ out_logprob,
                           float *__restrict__ out_logmass) {
+    griddep_launch_dependents();  // as in stage2_kernel
     griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t b = static_cast<int64_t>(blockIdx.x) * kStage2Warps + (threadIdx.x >> 5);

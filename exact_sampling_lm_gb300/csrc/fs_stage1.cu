@@ -351,13 +351,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (CS > 1) cluster_sync();
     const uint32_t tmem_base = *tmem_slot;
 
+    // Programmatic dependent launch: everything above overlaps the previous
+    // kernel of the stream.  Before waiting for it, the producer also warms L2
+    // with the first W k-blocks of this CTA's first tile.  That is safe even if
+    // the previous kernel writes W, because L2 is where writes become visible
+    // and shared memory is filled only after the wait.  Every other global
+    // access (H, the temperatures, the workspace) comes after the wait.
+    if (warp == kWarpTma && lane == 0) {
+        prefetch_tmap(&tmH);
+        prefetch_tmap(&tmW64);
+        prefetch_tmap(&tmW16);
+        prefetch_tmap(CS > 1 ? &tmWhalf : &tmWfull);
+        if (ntiles > 0 && !(a.flags & 0x100u)) {
+            int v0, tn;
+            tile_geom(geom, 0, v0, tn);
+            const int nbox = (round_up16(tn) + 63) >> 6;  // 64-row boxes covering the tile
+            const int nwarm = min(nk, nst + 2);
+            int kb = kb_first;
+            for (int jj = 0; jj < nwarm; ++jj) {
+                for (int i = static_cast<int>(crank); i < nbox; i += CS)
+                    tma_prefetch_l2_2d(&tmW64, kb * kBK, v0 + i * 64);
+                if (++kb == nk) kb = 0;
+            }
+        }
+    }
+    griddep_wait();
+
     if (warp == kWarpTma) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            prefetch_tmap(&tmH);
-            prefetch_tmap(&tmW64);
-            prefetch_tmap(&tmW16);
-            prefetch_tmap(CS > 1 ? &tmWhalf : &tmWfull);
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_h = l2_policy_evict_last();
             const uint32_t h_bytes = static_cast<uint32_t>(a.h_box_rows) * (kBK * 2);
@@ -780,13 +802,16 @@ static cudaError_t launch_mode(const CUtensorMap &tmH, const WMaps &wm, const St
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // the prologue may overlap the previous kernel (see griddep_wait in the kernel)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, stage1_kernel<MODE, CS>, tmH, wm.w16, wm.w64, wm.w128,
                               wm.w256, a);
 }
