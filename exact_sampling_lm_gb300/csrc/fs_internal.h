@@ -31,7 +31,12 @@ constexpr int kCombineBytes = kColParts * kBM * 20;  // per-row results of the c
 // alignment slack, the barriers and the combine area leave: 4 stages for a
 // full batch tile, and more when a small batch shrinks each stage's H slot.
 constexpr int kSmemBytes = 232448;
-constexpr int kRingBytes = kSmemBytes - 1024 - 256 - kCombineBytes;
+// Barriers (256 B) and the combine area sit in front of the ring, rounded up
+// to the 1 KB swizzle atom; a small batch's MMA reads up to 8 KB in front of
+// its first H slot from there (see the kernel).
+constexpr int kPreRingBytes = (256 + kCombineBytes + 1023) & ~1023;
+constexpr int kRingBytes = kSmemBytes - 1024 - kPreRingBytes;
+static_assert(kPreRingBytes >= 64 * kBK * 2, "room for a 64-lane offset of the A operand");
 constexpr int kMaxStages = 8;
 static_assert(kStages * (kABytes + kBBytes) <= kRingBytes, "ring of full batch tiles");
 constexpr int kFinalTileUnits = 8;  // last tile of a partition: 128 rows

@@ -285,18 +285,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
-    // Ring layout: nst H slots of a_stride bytes, then nst W slots.  A single
-    // batch tile loads only round_up(B, 8) rows of H per stage, so its H slot
-    // shrinks to that (in 1 KB swizzle atoms) and the ring holds more stages
-    // of W: 6 at B <= 16, 5 at B <= 88, else 4.  The MMA still reads 128 rows
-    // of A from the slot's start; the rows past the batch come from the next
-    // slots, stay inside the ring and feed accumulator lanes that no epilogue
-    // warp reads.
+    // Shared memory: barriers and the combine area, then the ring: nst H
+    // slots of a_stride bytes, then nst W slots.  A single batch tile loads
+    // only round_up(B, 8) rows of H per stage, so its H slot shrinks to that
+    // (in 1 KB swizzle atoms) and the ring holds more stages of W: 6 at
+    // B <= 16, 5 at B <= 88, else 4.
+    // A single batch tile of at most 64 (96) rows also sits in accumulator
+    // lanes 64.. (32..): the MMA's A descriptor starts lane_off rows (128 B
+    // each) before the H slot.  TMEM lane quarter q is read by the warps of SM
+    // sub-partition q, so the epilogue of a small batch then runs on
+    // sub-partitions 2-3, away from the TMA producer (0) and the MMA issuer
+    // (1).  The A rows the MMA reads around the batch come from neighbouring
+    // slots or from the area in front of the ring, always inside shared
+    // memory, and feed lanes that no epilogue warp reads.
     const int a_stride = (a.nM == 1) ? (a.h_box_rows * (kBK * 2) + 1023) & ~1023 : kABytes;
     const int nst = min(kMaxStages, kRingBytes / (a_stride + kBBytes));
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + nst * a_stride;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kRingBytes);
+    const int lane_off = (a.nM != 1) ? 0 : (a.B <= 64 ? 64 : (a.B <= 96 ? 32 : 0));
+    uint8_t *sA = smem + kPreRingBytes;
+    uint8_t *sB = sA + nst * a_stride;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     uint64_t *full_bar = bars;
     uint64_t *empty_bar = bars + kMaxStages;
     uint64_t *tfull_bar = bars + 2 * kMaxStages;
@@ -464,7 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(sA));
+            // lane_off rows before the H slot: H row r feeds accumulator lane lane_off + r
+            const uint64_t a_desc0 =
+                sw128_kmajor_desc(smem_u32(sA) - static_cast<uint32_t>(lane_off * (kBK * 2)));
             const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(sB));
             for (int t = 0; t < ntiles && ok; ++t) {
                 const int acc = t & 1;
@@ -514,10 +523,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue warps
         const int q = warp & 3;   // TMEM lane quarter (the warp's rank in its warpgroup)
         const int j = warp >> 2;  // column part of the tile
-        const int row = q * 32 + lane;
+        const int tl = q * 32 + lane;  // TMEM lane = accumulator row
+        const int row = tl - lane_off;  // row within the batch tile
         const int b = m * kBM + row;
-        const bool warp_has_rows = (m * kBM + q * 32) < a.B;
-        const bool row_ok = b < a.B;
+        const bool warp_has_rows = q * 32 >= lane_off && (m * kBM + q * 32 - lane_off) < a.B;
+        const bool row_ok = row >= 0 && b < a.B;
         float invT = 0.0f;
         bool t_ok = false;
         if (kSample && row_ok) {
@@ -727,27 +737,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kSample) {
             // Combine the column parts' bests of each row (tie: lower index),
             // then one candidate per (row, partition).
-            comb_s[j * kBM + row] = best;
-            comb_i[j * kBM + row] = bidx;
+            comb_s[j * kBM + tl] = best;
+            comb_i[j * kBM + tl] = bidx;
             if (kLogprob) {
-                comb_lt[j * kBM + row] = best_lt;
-                comb_m[j * kBM + row] = lse_m;
-                comb_sum[j * kBM + row] = lse_s;
+                comb_lt[j * kBM + tl] = best_lt;
+                comb_m[j * kBM + tl] = lse_m;
+                comb_sum[j * kBM + tl] = lse_s;
             }
             epilogue_barrier();
             if (j == 0 && row_ok) {
 #pragma unroll
                 for (int jj = 1; jj < kColParts; ++jj) {
-                    const float s = comb_s[jj * kBM + row];
-                    const int i = comb_i[jj * kBM + row];
+                    const float s = comb_s[jj * kBM + tl];
+                    const int i = comb_i[jj * kBM + tl];
                     if (s > best ||
                         (s == best && static_cast<uint32_t>(i) < static_cast<uint32_t>(bidx))) {
                         best = s;
                         bidx = i;
-                        if (kLogprob) best_lt = comb_lt[jj * kBM + row];
+                        if (kLogprob) best_lt = comb_lt[jj * kBM + tl];
                     }
                     if (kLogprob)
-                        lse_merge(lse_m, lse_s, comb_m[jj * kBM + row], comb_sum[jj * kBM + row]);
+                        lse_merge(lse_m, lse_s, comb_m[jj * kBM + tl], comb_sum[jj * kBM + tl]);
                 }
                 const size_t o = static_cast<size_t>(part) * a.B + b;
                 a.cand_score[o] = best;
