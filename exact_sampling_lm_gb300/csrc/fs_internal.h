@@ -20,11 +20,11 @@ constexpr int kStages = 4;
 constexpr int kUmmaK = 16;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KiB: H tile
 constexpr int kBBytes = kBN * kBK * 2;  // 32 KiB: W tile
-constexpr int kColParts = 4;                      // epilogue warps per TMEM lane quarter
-constexpr int kNumEpiWarps = 4 * kColParts;       // 16
-constexpr int kWarpTma = kNumEpiWarps;            // warp 16
-constexpr int kWarpMma = kNumEpiWarps + 1;        // warp 17
-constexpr int kThreads = (kNumEpiWarps + 2) * 32; // 576
+constexpr int kColParts = 4;                      // most epilogue warps per TMEM lane quarter
+constexpr int kNumEpiWarps = 14;                  // 3 + 3 + 4 + 4
+constexpr int kWarpTma = 12;                      // sub-partition 0
+constexpr int kWarpMma = 13;                      // sub-partition 1
+constexpr int kThreads = 16 * 32;                 // 512
 constexpr int kTmemCols = 512;  // two 256-column accumulators
 constexpr int kCombineBytes = kColParts * kBM * 20;  // per-row results of the column parts
 // Dynamic shared memory: the per-CTA maximum.  The ring takes what the

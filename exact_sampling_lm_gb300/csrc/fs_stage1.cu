@@ -8,23 +8,26 @@
 // chunk.  Only (score, index) candidates leave the chip, never the [B, V]
 // logits.
 //
-// GB300 design (one persistent CTA per SM, 576 threads = 18 warps):
-//   warp 16     TMA producer: streams H [rows x 64] and W [<=256 x 64] k-blocks
-//               (128-byte swizzled) into a 4-stage shared-memory ring; a whole
+// GB300 design (one persistent CTA per SM, 512 threads = 16 warps):
+//   warp 12     TMA producer: streams H [rows x 64] and W [<=256 x 64] k-blocks
+//               (128-byte swizzled) into a ring of 4-6 shared-memory stages; a whole
 //               W tile is one 256-row box (one 128-row box per CTA when
 //               paired), tails are 64- and 16-row boxes.
-//   warp 17     allocates 512 TMEM columns; one thread issues
+//   warp 13     allocates 512 TMEM columns; one thread issues
 //               tcgen05.mma (M=128, N<=256, K=16, bf16 -> f32) into one of two
 //               256-column accumulators and commits to mbarriers.
 //   The producer and the MMA issuer share SM sub-partitions 0 and 1 with
 //   busy epilogue warps, so they issue as few instructions per k-block as
 //   possible (whole-tile boxes, precomputed descriptors).
-//   warps 0-15  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//               lane quarter w % 4 and column quarter w / 4 of the tile), then
+//   warps 0-11, 14, 15  epilogue: tcgen05.ld of the accumulator (warp w reads
+//               TMEM lane quarter w % 4: three warps for quarters 0 and 1, which
+//               share their SM sub-partitions with the producer and the MMA
+//               issuer, four for quarters 2 and 3; each takes its share of the
+//               tile's columns), then
 //               per element s = l * (1/T) + g with g from Philox4x64-10, and a
 //               running per-row argmax across all tiles of the CTA.  The
 //               epilogue of tile t overlaps the MMA of tile t+1 (double-buffered
-//               TMEM).  At the end the four column quarters of each row are
+//               TMEM).  At the end the column parts of each row are
 //               merged through shared memory.
 // Batch rows sit on the MMA M dimension, so each epilogue thread owns one row
 // and scans its columns in increasing order: the lowest-index tie rule and
@@ -122,12 +125,14 @@ __device__ __forceinline__ void tile_geom(const PartGeom &g, int t, int &v0, int
     }
 }
 
-// First column of column part j (of kColParts) of a tile of width tn: parts
-// start on 16-column boundaries; part kColParts ends at tn.
-__device__ __forceinline__ int col_part_start(int j, int tn) {
-    if (j >= kColParts) return tn;
-    return min(tn, round_up16((j * tn + kColParts - 1) / kColParts));
+// First column of column part j (of np) of a tile of width tn: parts start
+// on 16-column boundaries; part np ends at tn.
+__device__ __forceinline__ int col_part_start(int j, int tn, int np) {
+    if (j >= np) return tn;
+    return min(tn, round_up16((j * tn + np - 1) / np));
 }
+// epilogue warps (column parts) of TMEM lane quarter q
+__device__ __forceinline__ int quarter_parts(int q) { return q < 2 ? 3 : 4; }
 
 // Element i (0..15) of a register array, by a chain of selects (an indexed
 // load would move the array to local memory).
@@ -337,11 +342,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Only epilogue warps whose TMEM lane quarter holds live batch rows
         // take part in the tile loop and release the accumulators.
-        const int live_rows = min(kBM, a.B - m * kBM);
-        const int live_quarters = (live_rows + 31) / 32;
+        int live_warps = 0;
+        for (int qq = 0; qq < 4; ++qq)
+            if (qq * 32 >= lane_off && (m * kBM + qq * 32 - lane_off) < a.B)
+                live_warps += quarter_parts(qq);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull_bar[i], 1);
-            mbar_init(&tempty_bar[i], kColParts * live_quarters);
+            mbar_init(&tempty_bar[i], live_warps);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -522,7 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------ epilogue warps
         const int q = warp & 3;   // TMEM lane quarter (the warp's rank in its warpgroup)
-        const int j = warp >> 2;  // column part of the tile
+        const int j = warp < 12 ? (warp >> 2) : 3;  // column part of the tile (warps 14, 15: 3)
+        const int np = quarter_parts(q);
         const int tl = q * 32 + lane;  // TMEM lane = accumulator row
         const int row = tl - lane_off;  // row within the batch tile
         const int b = m * kBM + row;
@@ -564,8 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
                 int v0p, tnp;
                 tile_geom(geom, t, v0p, tnp);
-                const int lo = col_part_start(j, tnp);
-                const int hi = col_part_start(j + 1, tnp);
+                const int lo = col_part_start(j, tnp, np);
+                const int hi = col_part_start(j + 1, tnp, np);
                 for (int c0 = lo; c0 < hi; c0 += 16) {
                     uint32_t wa[8], wb[8], w[16];
                     const uint64_t v8 = static_cast<uint64_t>(a.vocab_offset + v0p + c0) >> 3;
@@ -588,8 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             int v0, tn;
             tile_geom(geom, t, v0, tn);
-            const int c_lo = col_part_start(j, tn);
-            const int c_hi = col_part_start(j + 1, tn);
+            const int c_lo = col_part_start(j, tn, np);
+            const int c_hi = col_part_start(j + 1, tn, np);
             {
                 for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
                     uint32_t r[16];
@@ -747,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             epilogue_barrier();
             if (j == 0 && row_ok) {
 #pragma unroll
-                for (int jj = 1; jj < kColParts; ++jj) {
+                for (int jj = 1; jj < np; ++jj) {
                     const float s = comb_s[jj * kBM + tl];
                     const int i = comb_i[jj * kBM + tl];
                     if (s > best ||
