@@ -69,3 +69,17 @@ def test_reference_arm_other_ranks_exit_without_work():
                          capture_output=True, text=True, env=env, timeout=300)
     assert res.returncode == 0
     assert res.stdout.strip() == ""
+
+
+def test_kernel_hash_ignores_comments_and_whitespace():
+    """The traffic record is keyed by a hash of the kernel code: comment and
+    whitespace edits keep it, code edits (including string literals) change it."""
+    code = 'int f(int x) { return x + 1; }  // add one\n/* note */ const char *s = "a // b";\n'
+    same = '// header\nint f(int x) {\n    return x + 1;  /* add\n one */\n}\nconst char *s = "a // b";'
+    other = 'int f(int x) { return x + 2; }\nconst char *s = "a // b";\n'
+    lit = 'int f(int x) { return x + 1; }\nconst char *s = "a // c";\n'
+    assert bench._code_only(code) == bench._code_only(same)
+    assert bench._code_only(code) != bench._code_only(other)
+    assert bench._code_only(code) != bench._code_only(lit)
+    assert "add one" not in bench._code_only(code)
+    assert len(bench.kernel_source_hash()) == 16
