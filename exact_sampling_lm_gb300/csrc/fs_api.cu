@@ -496,6 +496,8 @@ struct HostPath {
     cudaStream_t copy = nullptr;
     cudaEvent_t uploaded[2] = {nullptr, nullptr};
     cudaEvent_t consumed[2] = {nullptr, nullptr};
+    cudaEvent_t all_prior = nullptr;      // everything queued on the caller's stream so far
+    bool kernel_upload[2] = {false, false};  // slot last filled by the upload kernel
     int next = 0;
     char *block = nullptr;
     size_t bytes = 0;
@@ -519,6 +521,8 @@ static fs_status host_path_ready(HostPath &h, size_t need, bool capturing) {
                     cudaSuccess)
                 return cuda_fail(e, "cudaEventCreate(upload events)");
         }
+        if ((e = cudaEventCreateWithFlags(&h.all_prior, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventCreate(upload events)");
     }
     if (h.bytes < need) {
         // cudaFree waits for all work on the device, including reads of the
@@ -574,10 +578,20 @@ fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V
     const size_t i_b = round256(ub * 8);
     const size_t s_b = round256(ub * 4);
 
-    // Under stream capture the upload stays on the caller's stream (a graph
-    // cannot wait on events recorded outside it); otherwise it runs on the
-    // internal upload stream and overlaps the previous call's kernels.
-    const bool overlap = !stream_capturing(s);
+    // Page-locked inputs are uploaded by a kernel on the caller's stream
+    // (upload_kernel): launched with programmatic serialization, it keeps the
+    // chain of back-to-back calls overlapping.  Pageable inputs are copied by
+    // the CUDA runtime: under stream capture on the caller's stream (a graph
+    // cannot wait on events recorded outside it), otherwise on the internal
+    // upload stream, overlapping the previous call's kernels.
+    const void *H_src = mapped_host_alias(const_cast<void *>(H_host));
+    const void *T_src =
+        temperatures_host ? mapped_host_alias(const_cast<float *>(temperatures_host)) : nullptr;
+    const bool by_kernel = H_src != nullptr && reinterpret_cast<uintptr_t>(H_src) % 16 == 0 &&
+                           (!temperatures_host ||
+                            (T_src != nullptr && reinterpret_cast<uintptr_t>(T_src) % 4 == 0));
+    const bool capturing = stream_capturing(s);
+    const bool overlap = !by_kernel && !capturing;
 
     HostPath *hp;
     {
@@ -587,7 +601,7 @@ fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V
     }
     HostPath &h = *hp;
     std::lock_guard<std::mutex> lock(h.mu);
-    if ((st = host_path_ready(h, 2 * (h_b + t_b) + i_b + s_b, !overlap)) != FS_OK) return st;
+    if ((st = host_path_ready(h, 2 * (h_b + t_b) + i_b + s_b, capturing)) != FS_OK) return st;
     cudaError_t e;
     const int j = h.next;
     h.next ^= 1;
@@ -597,18 +611,41 @@ fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V
     if (stage_idx) idx_dev = reinterpret_cast<int64_t *>(h.block + 2 * (h_b + t_b));
     if (stage_score) score_dev = reinterpret_cast<float *>(h.block + 2 * (h_b + t_b) + i_b);
 
-    cudaStream_t up = overlap ? h.copy : s;
-    if (overlap && (e = cudaStreamWaitEvent(up, h.consumed[j], 0)) != cudaSuccess)
-        return cuda_fail(e, "upload stream wait");
-    if ((e = cudaMemcpyAsync(H, H_host, h_bytes, cudaMemcpyDefault, up)) != cudaSuccess)
-        return cuda_fail(e, "upload of H");
-    if (T && (e = cudaMemcpyAsync(T, temperatures_host, ub * 4, cudaMemcpyDefault, up)) !=
-                 cudaSuccess)
-        return cuda_fail(e, "upload of the temperatures");
-    if (overlap) {
-        if ((e = cudaEventRecord(h.uploaded[j], up)) != cudaSuccess ||
-            (e = cudaStreamWaitEvent(s, h.uploaded[j], 0)) != cudaSuccess)
-            return cuda_fail(e, "upload ordering");
+    if (by_kernel) {
+        // Slot j was last read by the Stage 1 two calls back.  This kernel can
+        // start only once the previous call's Stage 2 has started, i.e. once
+        // every CTA of the previous Stage 1 has triggered its dependents --
+        // after its last load and after its own wait for the Stage 1 before.
+        if ((e = launch_upload(H_src, H, static_cast<int64_t>(h_bytes),
+                               static_cast<const float *>(T_src), T, T ? B : 0, s)) !=
+            cudaSuccess)
+            return cuda_fail(e, "upload kernel launch");
+        h.kernel_upload[j] = true;
+    } else {
+        cudaStream_t up = overlap ? h.copy : s;
+        if (overlap) {
+            // A slot last filled by the upload kernel recorded no release
+            // event: wait for everything queued so far instead.
+            cudaEvent_t ready = h.consumed[j];
+            if (h.kernel_upload[j]) {
+                if ((e = cudaEventRecord(h.all_prior, s)) != cudaSuccess)
+                    return cuda_fail(e, "upload ordering");
+                ready = h.all_prior;
+            }
+            if ((e = cudaStreamWaitEvent(up, ready, 0)) != cudaSuccess)
+                return cuda_fail(e, "upload stream wait");
+        }
+        if ((e = cudaMemcpyAsync(H, H_host, h_bytes, cudaMemcpyDefault, up)) != cudaSuccess)
+            return cuda_fail(e, "upload of H");
+        if (T && (e = cudaMemcpyAsync(T, temperatures_host, ub * 4, cudaMemcpyDefault, up)) !=
+                     cudaSuccess)
+            return cuda_fail(e, "upload of the temperatures");
+        if (overlap) {
+            if ((e = cudaEventRecord(h.uploaded[j], up)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(s, h.uploaded[j], 0)) != cudaSuccess)
+                return cuda_fail(e, "upload ordering");
+        }
+        h.kernel_upload[j] = false;
     }
     if ((st = fs_sample_ex(H, W, B, V, D, temperature, T, seed, offset, 0, idx_dev, score_dev,
                            nullptr, ws, p.wsBytes, stream)) != FS_OK)
@@ -893,6 +930,7 @@ fs_status fs_release_workspaces(void) {
             if (h.uploaded[j]) cudaEventDestroy(h.uploaded[j]);
             if (h.consumed[j]) cudaEventDestroy(h.consumed[j]);
         }
+        if (h.all_prior) cudaEventDestroy(h.all_prior);
         if (h.copy) cudaStreamDestroy(h.copy);
     }
     g_host.clear();

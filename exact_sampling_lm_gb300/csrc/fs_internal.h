@@ -129,6 +129,8 @@ cudaError_t launch_logits_sample(const void *Y, int y_dtype, int64_t B, int64_t 
                                  uint64_t offset, uint32_t flags, float *cand_score,
                                  int32_t *cand_idx, int nChunks, cudaStream_t stream);
 
+cudaError_t launch_upload(const void *src, void *dst, int64_t bytes, const float *tsrc,
+                          float *tdst, int64_t nt, cudaStream_t stream);
 cudaError_t launch_debug_gumbel(const uint32_t *words, int64_t n, float *out_g,
                                 cudaStream_t stream);
 cudaError_t launch_debug_noise(uint64_t seed, uint64_t offset, int64_t b0, int64_t nb,

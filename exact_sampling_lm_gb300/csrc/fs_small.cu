@@ -94,6 +94,48 @@ cudaError_t launch_stage2(const float *cand_score, const int32_t *cand_idx, int 
                               temp_scalar, out_idx, out_score);
 }
 
+// ------------------------------------------------------------------ host-buffer upload
+// Copies a call's H (n16 16-byte units) and per-row temperatures (nt floats)
+// from page-locked host memory, through its mapped device address, into the
+// call's device slot.  Launched with programmatic serialization and
+// triggering its dependents at once: it reads only host memory written before
+// the call and writes a slot that the Stage 1 two calls back has finished
+// loading (that Stage 1 triggered the Stage 2 whose start let this kernel
+// launch), so it needs no wait; the next Stage 1 waits for it before reading
+// the slot.
+__global__ void upload_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int64_t n16,
+                              const float *__restrict__ tsrc, float *__restrict__ tdst,
+                              int64_t nt) {
+    griddep_launch_dependents();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+         i += stride)
+        dst[i] = src[i];
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nt;
+         i += stride)
+        tdst[i] = tsrc[i];
+}
+
+cudaError_t launch_upload(const void *src, void *dst, int64_t bytes, const float *tsrc,
+                          float *tdst, int64_t nt, cudaStream_t stream) {
+    const int64_t n16 = bytes / 16;
+    int64_t blocks = (n16 + 255) / 256;
+    if (blocks > 256) blocks = 256;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, upload_kernel, static_cast<const uint4 *>(src),
+                              static_cast<uint4 *>(dst), n16, tsrc, tdst, nt);
+}
+
 // ------------------------------------------------------------------ Stage 2 with log-mass
 // Besides the argmax, each row merges the partitions' log-masses
 // (m_j, s_j) = (max l~, sum exp(l~ - max)) over the finite l~ into

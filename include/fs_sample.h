@@ -120,17 +120,21 @@ fs_status fs_sample(const void *H, const void *W, int64_t B, int64_t V, int64_t 
  *                     of this call (cudaStreamSynchronize or an event)
  *   out_score_host    NULL or host f32 [B], as out_idx_host
  * Order of work: H (and the temperatures) are copied into one of two device
- * slots used alternately, on an internal upload stream that waits for the
- * previous reader of that slot, so that the upload overlaps the previous
- * call's kernels; `stream` waits for the upload, then runs Stage 1 and
- * Stage 2.  Page-locked outputs are written by Stage 2 directly through their
- * mapped device address; pageable outputs are staged on the device and copied
- * back on `stream` (that copy completes before the call returns).  Page-locked
- * inputs keep the upload asynchronous; pageable inputs are staged by the CUDA
- * runtime.  While `stream` is being captured into a CUDA graph, the upload is
- * issued on `stream` itself, every host buffer must be page-locked, and the
- * device staging must already exist from an earlier call of the same size
- * on that stream (else FS_ERR_UNSUPPORTED, as for fs_sample).
+ * slots used alternately, then `stream` runs Stage 1 and Stage 2.
+ *   - Page-locked inputs (16-byte aligned H) are copied by a small kernel on
+ *     `stream` that reads them through their mapped device address.  It is
+ *     launched with programmatic dependent launch like both stages, so
+ *     back-to-back calls keep overlapping their set-up.
+ *   - Pageable inputs are copied by the CUDA runtime (staged before the call
+ *     returns) on an internal upload stream that waits for the previous reader
+ *     of the slot; `stream` waits for that copy.
+ * Page-locked outputs are written by Stage 2 directly through their mapped
+ * device address; pageable outputs are staged on the device and copied back
+ * on `stream` (that copy completes before the call returns).  While `stream`
+ * is being captured into a CUDA graph, pageable inputs are copied on `stream`
+ * itself (page-locked buffers are recommended), and the device staging must
+ * already exist from an earlier call of the same size on that stream (else
+ * FS_ERR_UNSUPPORTED, as for fs_sample).
  * Device state (upload stream, events, slots) is cached per (device, stream)
  * and freed by fs_release_workspaces().  Host pointers need no particular
  * alignment beyond their element size for page-locked outputs.  Results are

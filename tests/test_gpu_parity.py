@@ -281,6 +281,32 @@ def test_host_buffer_entry(fs, dev):
     compare_indices(ti.numpy(), o_idx, o_best, o_second, "host buffers")
 
 
+def test_host_buffer_entry_mixed_upload_paths(fs, dev):
+    """Page-locked inputs are uploaded by a kernel on the caller's stream,
+    pageable ones by a copy on an internal stream; back-to-back calls that
+    alternate between the two (no synchronisation in between) reuse the two
+    device slots safely and each equals fs_sample on the same data."""
+    g = torch.Generator(device="cpu").manual_seed(48)
+    B, V, D = 40, 20011, 136
+    W = (torch.randn((V, D), generator=g) * 0.09).to(torch.bfloat16).to(dev)
+    Hs = [torch.randn((B, D), generator=g).to(torch.bfloat16) for _ in range(7)]
+    T = 0.5 + torch.rand(B, generator=g)
+    refs = [fs.fs_sample(H.to(dev), W, temperature=T.to(dev), seed=9, offset=k)[0].cpu()
+            for k, H in enumerate(Hs)]
+    outs = []
+    for k, H in enumerate(Hs):
+        pinned = k % 3 != 1
+        Hk = H.pin_memory() if pinned else H.clone()
+        Tk = T.pin_memory() if pinned else T.clone()
+        idx = torch.empty(B, dtype=torch.int64).pin_memory()
+        fs.fs_sample_host(Hk, W, temperature=Tk, seed=9, offset=k, out_idx=idx,
+                          want_score=False)
+        outs.append((Hk, Tk, idx))
+    torch.cuda.synchronize()
+    for k, (_, _, idx) in enumerate(outs):
+        assert torch.equal(refs[k], idx), k
+
+
 def test_host_buffer_entry_growth_and_graph_capture(fs, dev):
     """fs_sample_host grows its staging between batch sizes, and under CUDA
     graph capture (upload on the captured stream) replays to the same draw."""
