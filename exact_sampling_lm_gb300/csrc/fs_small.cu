@@ -1,12 +1,16 @@
 // fs_small.cu -- the small kernels around Stage 1:
 //   * Stage 2 ("FlashSampling: Fast and Memory-Efficient Exact Sampling",
-//     method section, "Stage 2 (Reduction)"): argmax over the candidate
-//     buffer of shape [candidate slots, B], one warp per row;
+//     method section, Stage 2): argmax over the candidate buffer of shape
+//     [candidate slots, B], one warp per row; a variant that also merges the
+//     partitions' log-masses into the sampled token's log-probability;
+//   * the group combine of grouped sampling (a group drawn by its log-mass);
 //   * the sampling pass of the unfused comparator (the IO-model section's
-//     baseline: "sample from the logits" after a GEMM materialised them);
-//   * a debug kernel exposing the epilogue's noise for tests.
-// All of them use the same noise functions and tie rule as Stage 1: higher
-// score wins, equal scores go to the lower vocabulary index, NaN never wins.
+//     baseline, which samples from logits that a GEMM has written out);
+//   * the upload of a host-buffer call's page-locked inputs;
+//   * debug kernels exposing the epilogue's noise functions for tests.
+// All sampling kernels use the same noise functions and tie rule as Stage 1:
+// higher score wins, equal scores go to the lower vocabulary index, NaN never
+// wins.
 #include <cuda_bf16.h>
 #include <math.h>
 

@@ -5,8 +5,8 @@
  * The operation ("FlashSampling: Fast and Memory-Efficient Exact Sampling",
  * arXiv 2603.15854):
  *   - the LM-head GEMM l = H W^T with H [B, D] hidden states and W [V, D]
- *     vocabulary-major weights, both bf16 (experimental setup: "Inputs and
- *     weights are in BF16");
+ *     vocabulary-major weights, both bf16 (the experimental setup's
+ *     precision);
  *   - exact categorical sampling from softmax(l / T) by the Gumbel-max trick:
  *     draw i.i.d. Gumbels g, form s = l/T + g, return argmax s (method
  *     section, Algorithm I.1 of the Appendix);
@@ -188,7 +188,7 @@ fs_status fs_stage2(int64_t B, int64_t V, int64_t D, float temperature,
  *   out_logprob[b] = l~[idx] - log sum_v exp(l~[v]).
  * Stage 1 keeps, besides the per-row maximizer, each partition's log-mass
  * (max l~, sum exp(l~ - max)) -- the online-normalizer analogy of the method
- * section and the "local sample and local log-mass" summaries of the grouped /
+ * section and the per-shard sample plus log-mass of the grouped /
  * tensor-parallel variant (Section 4) -- and Stage 2 merges them over the
  * whole vocabulary.  Elements with a non-finite l~ are left out of the sum; a
  * row whose sampled l~ is not finite, or with an invalid temperature, gets
@@ -207,8 +207,8 @@ fs_status fs_sample_logprob(const void *H, const void *W, int64_t B, int64_t V, 
 /* ---------------------------------------------------------------------------
  * fs_sample_transformed -- the fused path with deterministic transforms
  * applied to the f32 logits in the Stage 1 epilogue, before the temperature
- * (method section: Stage 1 "applies deterministic transforms"; the pages do
- * not list them).  In this order, each rounded to f32:
+ * (method section: Stage 1 applies deterministic transforms before the
+ * noise; the pages do not list them).  In this order, each rounded to f32:
  *   l' = l + bias[v]                   bias: nullable device f32 [V], 16-byte aligned
  *   l' = c * tanh(l' / c)   if c > 0   softcap: logit soft-capping (0 = off)
  *   l' = -inf               where bit (v & 31) of allow_mask[b * mask_words + (v >> 5)]
@@ -238,7 +238,7 @@ fs_status fs_sample_transformed(const void *H, const void *W, int64_t B, int64_t
 /* ---------------------------------------------------------------------------
  * Grouped (hierarchical) sampling -- the pages' variant for online and
  * tensor-parallel settings (abstract; Section 4: each vocabulary shard returns
- * "a local sample and a local log-mass"), exact by the hierarchical
+ * its own sample and log-mass), exact by the hierarchical
  * factorisation P(v) = P(group(v)) P(v | group(v)).
  *
  * fs_sample_shard   the fused path over one vocabulary shard W_shard

@@ -10,7 +10,7 @@
  *  - the Gumbel-max rule of the method section: draw i.i.d. Gumbels g_i, form
  *    s_i = l~_i + g_i and return argmax_i s_i (the pages point to Algorithm I.1
  *    of the Appendix for it);
- *  - "a full Gumbel-Max pass" over the whole vocabulary: the paper's exactness
+ *  - one untiled Gumbel-max over the whole vocabulary: the paper's exactness
  *    statement (tiled argmax gives the same maximizer, Appendix C) means the
  *    reference result is the full, untiled pass, which is what is written here;
  *  - l = H W^T of the LM head (Section 3 IO model: the GEMM reads W and H);
@@ -279,8 +279,8 @@ void oracle_sample(const uint16_t *H, const uint16_t *W, int64_t B, int64_t V,
  * Log-probability of a sampled token under softmax(l~): l~[idx] - log sum_v
  * exp(l~[v]), with l~ = fl(l * fl(1/T)) in f32 as in the sampling pass and the
  * log-sum-exp evaluated in fp64 as (l~[idx] - max) - log sum exp(l~ - max).  This is the
- * "local log-mass" summary the grouped / tensor-parallel variant returns per
- * shard, reduced here over the whole vocabulary.  Reading for non-finite
+ * per-shard log-mass that the grouped / tensor-parallel variant returns,
+ * reduced here over the whole vocabulary.  Reading for non-finite
  * values (the pages are silent): the log-mass runs over the finite l~ only,
  * and a sampled token whose l~ is not finite gets NaN.  For each row of f32 logits
  * [B, V]: out[b] = logprob of idx[b] (NaN when idx[b] < 0 or T[b] invalid).
@@ -312,9 +312,9 @@ void oracle_logprob(const float *logits, int64_t B, int64_t V, const float *T,
 
 /* ---------------------------------------------------------------------------
  * Deterministic transforms applied to the f32 logits before the temperature
- * (method section: Stage 1 "applies deterministic transforms"; the pages do
- * not list them -- this library offers the common ones), in this order, each
- * rounded to f32:
+ * (method section: Stage 1 applies deterministic transforms before the noise;
+ * the pages do not list them -- this library offers the common ones), in this
+ * order, each rounded to f32:
  *   l' = l + bias[v]                         (bias may be NULL)
  *   l' = c * tanh(l' / c)      if c > 0      (logit soft-capping)
  *   l' = -inf                  if mask given and bit (v & 31) of
