@@ -78,6 +78,7 @@ __device__ __forceinline__ int round_up16(int x) { return (x + 15) & ~15; }
 // multiples of 16 rows.
 struct PartGeom {
     int r0, r1, nu, nmain, ntiles;
+    int base, extra;  // balanced split: the first `extra` main tiles have base + 1 units
 };
 
 __device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V, bool full_tiles) {
@@ -98,6 +99,8 @@ __device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V, boo
     } else {
         g.nmain = (g.nu - kFinalTileUnits + kTileUnits - 1) / kTileUnits;
         g.ntiles = g.nmain + 1;
+        g.base = (g.nu - kFinalTileUnits) / g.nmain;
+        g.extra = (g.nu - kFinalTileUnits) % g.nmain;
     }
     return g;
 }
@@ -113,14 +116,13 @@ __device__ __forceinline__ void tile_geom(const PartGeom &g, int t, int &v0, int
         tn = g.r1 - g.r0;
         return;
     }
-    const int main_units = g.nu - kFinalTileUnits;
+    // Tile t starts at unit t * base + min(t, extra): no product above the
+    // partition's own unit count, so no overflow for any V < 2^31.
     if (t < g.nmain) {
-        const int s = main_units * t / g.nmain;
-        const int e = main_units * (t + 1) / g.nmain;
-        v0 = g.r0 + kUnitRows * s;
-        tn = kUnitRows * (e - s);
+        v0 = g.r0 + kUnitRows * (t * g.base + min(t, g.extra));
+        tn = kUnitRows * (g.base + (t < g.extra ? 1 : 0));
     } else {
-        v0 = g.r0 + kUnitRows * main_units;
+        v0 = g.r0 + kUnitRows * (g.nu - kFinalTileUnits);
         tn = g.r1 - v0;
     }
 }

@@ -764,3 +764,55 @@ def test_edge_sizes(fs, dev):
     H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
     W = (torch.randn((V, D), generator=g) * 0.5).to(torch.bfloat16).to(dev)
     run_and_check(fs, H, W, 1.0, 7, 8, "V=2^21", store=False)
+
+
+def test_maximum_vocabulary(fs, dev):
+    """V = 2^31 - 1, the largest vocabulary the ABI accepts: 34 GB of W at
+    D = 8, a 14 M-row partition per CTA (55 K tiles).  Every row of W is zero
+    except two whose logit is 64, one of them the very last row (inside the
+    ragged last 16-row unit).  Their scores (>= 61) beat every other element
+    (l + g <= 16.7), so the sample is whichever of the two draws the larger
+    Gumbel.  The oracle draws those two Gumbels one by one and decides; over
+    eight offsets each token wins at least once, and every decision and
+    winning score match."""
+    V, D = (1 << 31) - 1, 8
+    hot = (1000, V - 1)
+    seed = 0x5EED7777
+    W = torch.zeros((V, D), dtype=torch.bfloat16, device=dev)
+    try:
+        for v in hot:
+            W[v, 0] = 8.0
+        H = torch.zeros((1, D), dtype=torch.bfloat16, device=dev)
+        H[0, 0] = 8.0
+        wins = set()
+        for off in range(8):
+            idx, score = fs.fs_sample(H, W, temperature=1.0, seed=seed, offset=off)
+            torch.cuda.synchronize()
+            assert fs.fs_get_device_status() == 0
+            s = [np.float32(np.float32(64.0) + np.float32(oracle.gumbel(seed, off, 0, v)))
+                 for v in hot]
+            expect = hot[0] if s[0] >= s[1] else hot[1]
+            got = int(idx[0])
+            if abs(float(s[0]) - float(s[1])) >= NEAR_TIE:
+                assert got == expect, "offset %d: sampled %d, oracle %d" % (off, got, expect)
+            else:
+                assert got in hot
+            assert abs(float(score[0]) - float(max(s))) <= 2e-5
+            wins.add(got)
+        assert wins == set(hot)
+    finally:
+        del W
+        torch.cuda.empty_cache()
+
+
+def test_huge_batch_with_large_vocabulary(fs, dev):
+    """B = 19201 (151 batch tiles, the last holding one row) and V = 3,200,011:
+    one vocabulary partition per batch tile, so each CTA streams all of W in
+    12,500 balanced tiles.  Sampled rows against the oracle, among them the
+    single row of the last batch tile."""
+    B, V, D = 19201, 3_200_011, 8
+    g = torch.Generator(device="cpu").manual_seed(4242)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.7).to(torch.bfloat16).to(dev)
+    rows = np.array([0, 1, 127, 128, 9600, 19199, 19200])
+    run_and_check(fs, H, W, 0.9, 11, 12, "B=%d V=%d" % (B, V), store=False, rows=rows)
