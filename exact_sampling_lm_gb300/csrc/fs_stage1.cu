@@ -78,7 +78,6 @@ __device__ __forceinline__ int round_up16(int x) { return (x + 15) & ~15; }
 // multiples of 16 rows.
 struct PartGeom {
     int r0, r1, nu, nmain, ntiles;
-    int base, extra;  // balanced split: the first `extra` main tiles have base + 1 units
 };
 
 __device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V, bool full_tiles) {
@@ -99,8 +98,6 @@ __device__ __forceinline__ PartGeom part_geom(int64_t u0, int64_t u1, int V, boo
     } else {
         g.nmain = (g.nu - kFinalTileUnits + kTileUnits - 1) / kTileUnits;
         g.ntiles = g.nmain + 1;
-        g.base = (g.nu - kFinalTileUnits) / g.nmain;
-        g.extra = (g.nu - kFinalTileUnits) % g.nmain;
     }
     return g;
 }
@@ -116,13 +113,17 @@ __device__ __forceinline__ void tile_geom(const PartGeom &g, int t, int &v0, int
         tn = g.r1 - g.r0;
         return;
     }
-    // Tile t starts at unit t * base + min(t, extra): no product above the
+    // Balanced split: the first `extra` main tiles take base + 1 units.  Tile
+    // t starts at unit t * base + min(t, extra); no product exceeds the
     // partition's own unit count, so no overflow for any V < 2^31.
+    const int main_units = g.nu - kFinalTileUnits;
     if (t < g.nmain) {
-        v0 = g.r0 + kUnitRows * (t * g.base + min(t, g.extra));
-        tn = kUnitRows * (g.base + (t < g.extra ? 1 : 0));
+        const int base = main_units / g.nmain;
+        const int extra = main_units - base * g.nmain;
+        v0 = g.r0 + kUnitRows * (t * base + min(t, extra));
+        tn = kUnitRows * (base + (t < extra ? 1 : 0));
     } else {
-        v0 = g.r0 + kUnitRows * (g.nu - kFinalTileUnits);
+        v0 = g.r0 + kUnitRows * main_units;
         tn = g.r1 - v0;
     }
 }
