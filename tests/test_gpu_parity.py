@@ -711,6 +711,28 @@ def test_shards_and_grouped_combine(fs, dev, B, V, D, cuts):
     print("[grouped B=%d V=%d] group near-ties %d, mismatches %d" % (B, V, int(grp_near.sum()), int(gm.sum())))
 
 
+def test_shard_at_the_top_of_the_index_range(fs, dev):
+    """A ragged shard whose last row has global index 2^31 - 2, the largest
+    the ABI accepts (offset + rows <= 2^31 - 1): local samples (global
+    indices and noise) and log-masses against the oracle; one more row is
+    refused."""
+    B, Vs, D = 9, 5003, 64
+    off0 = ((1 << 31) - Vs) // 16 * 16
+    Vs = (1 << 31) - 1 - off0  # last global index 2^31 - 2
+    g = torch.Generator(device="cpu").manual_seed(31)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((Vs, D), generator=g) * (2.0 / D ** 0.5)).to(torch.bfloat16).to(dev)
+    i, sc, lm = fs.fs_sample_shard(H, W, off0, temperature=0.8, seed=5, offset=6)
+    torch.cuda.synchronize()
+    oi, osc, olm, osec = oracle.sample_shard(bits(H), bits(W), off0, host_T(0.8, B), 5, 6)
+    compare_indices(i.cpu().numpy(), oi, osc, osec, "shard [%d, 2^31)" % off0)
+    assert np.all(np.abs(lm.cpu().numpy() - olm) <= 2 * LOGIT_TOL / 0.8 + 1e-4)
+    assert Vs % 16 != 0 and int(i.max()) <= (1 << 31) - 2 and int(i.min()) >= off0
+    W2 = torch.zeros((Vs + 1, D), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(fs.FSError):
+        fs.fs_sample_shard(H, W2, off0, temperature=0.8, seed=5, offset=6)
+
+
 # ---------------------------------------------------------------- exactness of the law, edge sizes
 
 def _chisq_p(counts, probs):
@@ -764,6 +786,31 @@ def test_edge_sizes(fs, dev):
     H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
     W = (torch.randn((V, D), generator=g) * 0.5).to(torch.bfloat16).to(dev)
     run_and_check(fs, H, W, 1.0, 7, 8, "V=2^21", store=False)
+
+
+def test_maximum_batch_and_hidden_size(fs, dev):
+    """B = 2^24 and D = 2^20, the largest the ABI accepts (each with a small
+    other dimension): sampled rows against the oracle, among them the last
+    row of the batch; one more row or 8 more columns are refused."""
+    g = torch.Generator(device="cpu").manual_seed(2024)
+    # B = 2^24: 131072 batch tiles in CTA pairs, one 24-row vocabulary tile
+    B, V, D = 1 << 24, 24, 8
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.6).to(torch.bfloat16).to(dev)
+    rows = np.array([0, 1, 129, 1 << 23, B - 2, B - 1])
+    run_and_check(fs, H, W, 1.1, 21, 22, "B=2^24", store=False, rows=rows)
+    with pytest.raises(fs.FSError):
+        fs.fs_sample(torch.zeros((B + 1, D), dtype=torch.bfloat16, device=dev), W)
+    del H
+    # D = 2^20: 16384 k-blocks per tile, W rows of 2 MB
+    B, V, D = 3, 40, 1 << 20
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * (1.0 / D ** 0.5)).to(torch.bfloat16).to(dev)
+    run_and_check(fs, H, W, 0.5, 23, 24, "D=2^20")
+    with pytest.raises(fs.FSError):
+        fs.fs_sample(torch.zeros((B, D + 8), dtype=torch.bfloat16, device=dev),
+                     torch.zeros((V, D + 8), dtype=torch.bfloat16, device=dev))
+    torch.cuda.empty_cache()
 
 
 def test_maximum_vocabulary(fs, dev):
