@@ -157,37 +157,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// Screening threshold of the argmax.  An element with transformed logit lt
-// can only beat the running best `best` if its Gumbel exceeds d = best - lt,
-// i.e. if u > F(d) = exp(-exp(-d)) (Gumbel CDF).  This returns a value that
-// is never above exp(-exp(kScreenSlack - d)) <= F(d - kScreenSlack): the
-// slack absorbs the f32 roundings of d, of s = lt + g and of the computed g,
-// and the factor (1 - 2^-12) absorbs the relative error of the two nested
-// hardware exp2 approximations (about e1 * 1.8e-6 + 2.4e-7 for e1 =
-// exp(slack - d); below 2^-12 for every e1 <= 133, and for larger e1 the
-// true threshold is under 2^-190, far below the smallest u = 2^-24).  The
-// computed g (gumbel_from_word) is within a few 1e-6 of the true Gumbel, far
-// inside the slack.  Elements with u <= threshold cannot win and skip
-// gumbel_from_word; the others take the exact path, so the result equals the
-// unscreened scan.  Non-finite cases: best = -inf gives 0
-// (always exact path); NaN d gives NaN (comparison false: such an element
-// cannot win either).
-constexpr float kScreenSlack = 0x1p-10f;
-__device__ __forceinline__ float screen_threshold(float d) {
-    constexpr float kLog2e = 1.4426950408889634f;
-    const float e1 = ex2_approx(__fmul_rn(kLog2e, kScreenSlack - d));  // exp(slack - d)
-    const float thr = ex2_approx(-kLog2e * e1);                           // exp(-e1)
-    return thr * (1.0f - 0x1p-12f);
+// Screen of the argmax, one test per element.  An element with transformed
+// logit lt can beat the running best only if its Gumbel g = -log(w), with
+// w = -log(u), exceeds best - lt.  Because -log(u) >= 1 - u, w is at least
+// the tail 1 - u = 2^-24 (2^24 - k) >= 2^-23 e2, where e2 = (~x) >> 9 is the
+// top 23 bits of the complemented word (k = (x >> 8) | 1).  So the element
+// can win only if 2^-23 e2 < exp(lt - best), i.e. if
+//     lg2(e2) < (lt - best) log2(e) + 23.
+// screen_lg2_tail gives lg2(e2) from the hardware log2 (e2 = 0 gives -inf,
+// which always passes); screen_bound gives the right-hand side plus a margin
+// of 2^-8 in log2 units (2.7e-3 in natural units).  The margin covers the
+// computed Gumbel's error (a few 1e-6), the hardware log2's error (below 1e-5
+// for results up to 23), and the roundings of lt - best and of the fma, which
+// are tiny wherever |lt - best| is small enough for the test to be close.  A
+// rejected element therefore has lt + g < best in exact arithmetic, so its
+// rounded score cannot exceed best: the screened scan returns what the
+// unscreened one does.  Non-finite cases: best = -inf makes the bound +inf
+// (everything passes); a NaN lt - best fails the comparison, and such an
+// element could not win either.
+constexpr float kScreenBias = 23.0f + 0x1p-8f;
+
+__device__ __forceinline__ float screen_lg2_tail(uint32_t x) {
+    const uint32_t e2 = (~x) >> 9;                                   // below 2^23
+    const float f = __uint_as_float(0x4B000000u | e2) - 8388608.0f;  // e2, exactly
+    return lg2_approx(f);
 }
 
-// Integer form of the screen for a group of elements: the largest k with
-// k * 2^-24 <= screen_threshold(d), so that an element with 24-bit numerator
-// kx = (x >> 8) | 1 passes the screen iff kx > screen_kbound(d).  For NaN d
-// it returns 0 (every element takes the exact path).  A group of elements may
-// share one bound computed at the group's smallest d (largest transformed
-// logit): the threshold rises with d, so that bound is the most permissive.
-__device__ __forceinline__ uint32_t screen_kbound(float d) {
-    return __float2uint_rd(screen_threshold(d) * 0x1p24f);
+__device__ __forceinline__ float screen_bound(float lt, float best) {
+    return fmaf(lt - best, 1.4426950408889634f, kScreenBias);
 }
 
 }  // namespace fs

@@ -41,8 +41,8 @@
 // different k-block, so the CTAs do not all request the same H line from L2
 // at once.
 // The epilogue screens every element with a cheap conservative bound
-// (screen_kbound): only elements that may beat the running best pay for the
-// exact Gumbel, and the result equals the unscreened scan.
+// (screen_lg2_tail / screen_bound): only elements that may beat the running
+// best pay for the exact Gumbel, and the result equals the unscreened scan.
 //
 // Every wait is bounded: on expiry the CTA raises the device error word,
 // tells its other warps to stop, drains its own TMA loads and MMAs, frees TMEM
@@ -653,21 +653,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (n_valid > 8) noise_words8(prow, v8 + 1, xb);
                                 }
                                 float lt[16];
-                                float lmax_a = -INFINITY, lmax_b = -INFINITY;
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) {
+                                for (int i = 0; i < 16; ++i)
                                     lt[i] = __fmul_rn(__uint_as_float(r[i]), invT);
-                                    if (i < n_valid) {
-                                        if (i < 8)
-                                            lmax_a = fmaxf(lmax_a, lt[i]);
-                                        else
-                                            lmax_b = fmaxf(lmax_b, lt[i]);
-                                    }
-                                }
-                                // One conservative screen bound per group of 8,
-                                // against the best known before the chunk (a
-                                // lower bound of the running best); survivors
-                                // are scanned exactly, in order.
+                                // A conservative screen per element against the
+                                // best known before the chunk (a lower bound of
+                                // the running best); survivors are scanned
+                                // exactly, in order.
                                 if (kLogprob) {
                                     // online log-sum-exp over the finite l~,
                                     // rescaled once per chunk
@@ -700,13 +692,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         }
                                     }
                                 } else {
-                                const uint32_t kb_a = screen_kbound(best0 - lmax_a);
-                                const uint32_t kb_b = screen_kbound(best0 - lmax_b);
                                 uint32_t pass = 0;
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) {
                                     const uint32_t xi = i < 8 ? xa[i] : xb[i - 8];
-                                    if (i < n_valid && ((xi >> 8) | 1u) > (i < 8 ? kb_a : kb_b))
+                                    if (i < n_valid &&
+                                        screen_lg2_tail(xi) < screen_bound(lt[i], best0))
                                         pass |= 1u << i;
                                 }
                                 // Exact scores only for the survivors, lowest
