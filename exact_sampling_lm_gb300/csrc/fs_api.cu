@@ -166,8 +166,29 @@ static EncodeTiledFn encode_fn() {
 
 // Row-major bf16 matrix [rows, cols] read in boxes of 64 columns x box_rows
 // rows, 128-byte swizzled in shared memory; out-of-range elements read as 0.
+// A tensor map depends only on (address, shape, box), and a decode loop keeps
+// passing the same few buffers, so each host thread keeps its most recent
+// encodings and copies a match instead of calling the driver again.
+struct TmapEntry {
+    const void *base = nullptr;
+    int64_t rows = 0, cols = 0;
+    uint32_t box_rows = 0;
+    CUtensorMap map;
+};
+constexpr int kTmapCacheSize = 16;
+static thread_local TmapEntry t_tmap_cache[kTmapCacheSize];
+static thread_local int t_tmap_next = 0;
+
 static fs_status make_tmap(CUtensorMap *map, const void *base, int64_t rows, int64_t cols,
                            uint32_t box_rows) {
+    for (int i = 0; i < kTmapCacheSize; ++i) {
+        const TmapEntry &e = t_tmap_cache[i];
+        if (e.base == base && e.base != nullptr && e.rows == rows && e.cols == cols &&
+            e.box_rows == box_rows) {
+            *map = e.map;
+            return FS_OK;
+        }
+    }
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(FS_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -181,6 +202,13 @@ static fs_status make_tmap(CUtensorMap *map, const void *base, int64_t rows, int
         return fail(FS_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld x %lld] box %u",
                     static_cast<int>(r), static_cast<long long>(rows),
                     static_cast<long long>(cols), box_rows);
+    TmapEntry &e = t_tmap_cache[t_tmap_next];
+    t_tmap_next = (t_tmap_next + 1) % kTmapCacheSize;
+    e.base = base;
+    e.rows = rows;
+    e.cols = cols;
+    e.box_rows = box_rows;
+    e.map = *map;
     return FS_OK;
 }
 
