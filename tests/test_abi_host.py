@@ -134,6 +134,29 @@ def test_other_entry_points_validate():
     assert L.fs_workspace_size(0, 64, 64) == 0
 
 
+def test_shard_and_combine_entries_validate():
+    """Vocabulary shards: the offset is a non-negative multiple of 16 and the
+    shard's last global index stays below 2^31 - 1; the grouped combine needs
+    at least one group and at most 2^24 rows.  All refused before any launch."""
+    L = _lib.lib()
+
+    def shard(vocab_offset, V=64, logmass=48):
+        return L.fs_sample_shard(16, 32, 4, V, 64, vocab_offset, 1.0, None, 0, 0, 16, None,
+                                 logmass, 64, 1 << 20, None)
+
+    assert shard(8) == _lib.FS_ERR_INVALID_ARG
+    assert shard(-16) == _lib.FS_ERR_INVALID_ARG
+    # offset + V = 2^31: the last global index would be 2^31 - 1 (every case
+    # here is refused by validation, so no call reaches a device)
+    assert shard(2**31 - 64, V=64) == _lib.FS_ERR_UNSUPPORTED
+    assert shard(2**31 - 80, V=80) == _lib.FS_ERR_UNSUPPORTED
+    assert shard(0, logmass=None) == _lib.FS_ERR_INVALID_ARG
+    assert shard(0, logmass=50) == _lib.FS_ERR_UNSUPPORTED         # misaligned log-mass output
+    assert L.fs_combine_groups(0, 4, 16, 32, 0, 0, 48, 64, None) == _lib.FS_ERR_INVALID_ARG
+    assert L.fs_combine_groups(2, 2**24 + 1, 16, 32, 0, 0, 48, 64, None) == _lib.FS_ERR_UNSUPPORTED
+    assert L.fs_combine_groups(2, 4, None, 32, 0, 0, 48, 64, None) == _lib.FS_ERR_INVALID_ARG
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
 def test_valid_call_without_a_device_reports_cuda_error():
     """With valid arguments but no GPU the call fails with FS_ERR_CUDA (or
