@@ -1,8 +1,11 @@
 """Write tests/golden/tiny_oracle.json from the CPU oracle alone.
 
-The fixture freezes the oracle's answer on the tiny workload (B=4, D=256,
-V=4096, T=1.0; inputs from the seeded generators in ``workloads``) so that a
-later change to the oracle's arithmetic shows up as a diff.  Run from the
+The fixture freezes the oracle's answers on the tiny workload (B=4, D=256,
+V=4096, T=1.0; inputs from the seeded generators in ``workloads``): the
+sample at two offsets, the logits, the sampled token's log-probability, a
+sample after bias / soft-cap / mask, three vocabulary shards and their
+grouped combine.  A later change to the oracle's arithmetic shows up as a
+diff.  Run from the
 repository root:  python tests/golden/make_golden.py
 """
 import hashlib
@@ -37,10 +40,30 @@ def input_digest(H, W):
     return h.hexdigest()
 
 
+def extra_inputs(B, V):
+    """Bias [V] in [-0.5, 0.5) and an allowed-token mask [B, ceil(V/32)], from
+    PCG64's raw output (stable across numpy versions)."""
+    raw = np.random.PCG64(2026).random_raw(V + B * ((V + 31) // 32))
+    bias = ((raw[:V] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53 - 0.5).astype(np.float32)
+    mask = (raw[V:] & np.uint64(0xFFFFFFFF)).astype(np.uint32).reshape(B, (V + 31) // 32)
+    return bias, mask
+
+
 def compute():
     H, W, T, seed, offset = tiny_inputs()
     idx, best, second, l64 = oracle.sample(H, W, T, seed, offset, want_logits=True)
     idx1, best1, second1, _ = oracle.sample(H, W, T, seed, offset + 1)
+    # the wider rows: log-probability of the sample, transforms, shards and
+    # the grouped combine, on the same inputs
+    l32 = oracle.logits(H, W).astype(np.float32)
+    lp = oracle.logprob(l32, T, idx)
+    bias, mask = extra_inputs(*l32.shape)
+    lx = oracle.transform_logits(l32, bias=bias, softcap=15.0, mask=mask)
+    xidx, xbest, _, _ = oracle.sample_from_logits(lx, T, seed, offset)
+    cuts = [(0, 1024), (1024, 3072), (3072, W.shape[0])]
+    shards = [oracle.sample_shard(H, W[a:b], a, T, seed, offset) for a, b in cuts]
+    gidx, grp = oracle.combine_groups(np.stack([s[0] for s in shards]),
+                                      np.stack([s[2] for s in shards]), 777, offset)
     return {
         "workload": "tiny B=4 D=256 V=4096 T=1.0",
         "inputs_sha256": input_digest(H, W),
@@ -51,6 +74,14 @@ def compute():
         "second": [[float(x) for x in second], [float(x) for x in second1]],
         "logits_row0_first8": [float(x) for x in l64[0, :8]],
         "logits_sum": float(np.sum(l64)),
+        "logprob": [float(x) for x in lp],
+        "xform_idx": xidx.tolist(),
+        "xform_best": [float(x) for x in xbest],
+        "shard_cuts": cuts,
+        "shard_idx": [s[0].tolist() for s in shards],
+        "shard_logmass": [[float(x) for x in s[2]] for s in shards],
+        "group_idx": gidx.tolist(),
+        "group": grp.tolist(),
     }
 
 

@@ -19,5 +19,6 @@ def test_tiny_golden():
     got = make_golden.compute()
     assert got["inputs_sha256"] == want["inputs_sha256"], (
         "the seeded tiny inputs changed (torch RNG?); regenerate the fixture")
-    for key in ("idx", "best", "second", "logits_row0_first8", "logits_sum"):
+    for key in ("idx", "best", "second", "logits_row0_first8", "logits_sum", "logprob",
+                "xform_idx", "xform_best", "shard_idx", "shard_logmass", "group_idx", "group"):
         assert got[key] == want[key], key
