@@ -370,6 +370,38 @@ def test_group_noise_is_separate_from_token_noise():
     assert np.count_nonzero(a == b) == 0
 
 
+def _tied_logmass(seed, offset, b, g_lo, g_hi):
+    """A log-mass for group g_hi whose f32 sum with its Gumbel equals group
+    g_lo's sum at log-mass 0, searched over a few floats around the
+    difference of the two Gumbels."""
+    G = [np.float32(oracle.group_gumbel(seed, offset, b, g)) for g in (g_lo, g_hi)]
+    target = np.float32(np.float32(0) + G[0])
+    x = np.float32(G[0] - G[1])
+    for k in range(-8, 9):
+        cand = np.float32(x + np.float32(k) * np.spacing(x))
+        if np.float32(cand + G[1]) == target:
+            return cand
+    raise AssertionError("no exact tie found")
+
+
+def test_group_ties_go_to_the_lower_group():
+    """Ties between groups' perturbed log-masses go to the lower group (the
+    same rule as for tokens); NaN and -inf log-masses never win."""
+    seed, offset = 12, 3
+    # row 0: groups 0 and 1 tie; row 1: groups 1 and 2 tie, group 0 is -inf
+    t01 = _tied_logmass(seed, offset, 0, 0, 1)
+    t12 = _tied_logmass(seed, offset, 1, 1, 2)
+    lm = np.array([[0.0, -np.inf], [t01, 0.0], [-np.inf, t12]], dtype=np.float32)
+    idx = np.array([[10, 20], [11, 21], [12, 22]], dtype=np.int64)
+    out, grp, best, second = oracle.combine_groups(idx, lm, seed, offset, want_scores=True)
+    assert best[0] == second[0] and best[1] == second[1]  # the ties are exact
+    assert list(grp) == [0, 1] and list(out) == [10, 21]
+    # NaN never wins, even against -inf; a row of only -inf / NaN has no group
+    lm2 = np.array([[np.nan, np.nan], [-np.inf, np.nan]], dtype=np.float32)
+    out2, grp2 = oracle.combine_groups(idx[:2], lm2, seed, offset)
+    assert list(grp2) == [-1, -1] and list(out2) == [-1, -1]
+
+
 @pytest.mark.parametrize("cuts", [(16,), (8, 40), (3, 5, 30, 31)])
 def test_grouped_sampler_matches_softmax(cuts):
     """Hierarchical factorisation: 10^5 grouped draws (rows as trials) follow
