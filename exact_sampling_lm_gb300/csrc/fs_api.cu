@@ -86,6 +86,7 @@ bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *p) {
     const int64_t slots = p->nCand > p->nChunks ? p->nCand : p->nChunks;
     const int64_t region = ((slots * B * 4) + 255) / 256 * 256;
     p->wsBytes = static_cast<size_t>(kWorkspaceRegions * region);
+    p->wsSampleBytes = static_cast<size_t>(2 * region);
     return true;
 }
 
@@ -162,6 +163,33 @@ static EncodeTiledFn encode_fn() {
             fn = reinterpret_cast<EncodeTiledFn>(p);
     });
     return fn;
+}
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+bool current_context_id(unsigned long long *id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+        cudaGetLastError();
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
 }
 
 // Row-major bf16 matrix [rows, cols] read in boxes of 64 columns x box_rows
@@ -264,13 +292,52 @@ static fs_status validate_temperature(float temperature, const float *temperatur
     return FS_OK;
 }
 
-static fs_status validate_workspace(const Plan &p, const void *ws, size_t bytes) {
+// need: p.wsSampleBytes for the calls that keep only (score, index)
+// candidates, p.wsBytes for the ones that also keep log-masses.
+static fs_status validate_workspace(const void *ws, size_t bytes, size_t need) {
     if (!ws) return fail(FS_ERR_INVALID_ARG, "workspace must be non-null");
     if (reinterpret_cast<uintptr_t>(ws) % 16)
         return fail(FS_ERR_UNSUPPORTED, "workspace must be 16-byte aligned");
-    if (bytes < p.wsBytes)
+    if (bytes < need)
         return fail(FS_ERR_NO_MEMORY, "workspace of %zu bytes is smaller than the %zu needed",
-                    bytes, p.wsBytes);
+                    bytes, need);
+    return FS_OK;
+}
+
+static const char *memory_type_name(cudaMemoryType t) {
+    switch (t) {
+        case cudaMemoryTypeHost: return "page-locked host memory";
+        case cudaMemoryTypeDevice: return "device memory";
+        case cudaMemoryTypeManaged: return "managed memory";
+        default: return "memory the CUDA runtime does not know";
+    }
+}
+
+// The TMA tensor maps of Stage 1 are encoded on the caller's H and W, and the
+// paired kernel multicasts each W box into both CTAs of a cluster.  Those
+// loads must read this GPU's own memory: not host memory reached through a
+// mapping, not another GPU's memory reached through peer access, not managed
+// memory that may migrate.  Anything else is refused before a launch.
+static fs_status require_local_device_memory(const void *p, const char *name) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    cudaPointerAttributes a;
+    e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer leaves no sticky error
+        return fail(FS_ERR_UNSUPPORTED, "%s is not memory the CUDA runtime knows (%s)", name,
+                    cudaGetErrorString(e));
+    }
+    if (a.type != cudaMemoryTypeDevice)
+        return fail(FS_ERR_UNSUPPORTED,
+                    "%s must be device memory of the current GPU; it is %s", name,
+                    memory_type_name(a.type));
+    if (a.device != dev)
+        return fail(FS_ERR_UNSUPPORTED,
+                    "%s is memory of GPU %d, but the current GPU is %d: Stage 1 reads its "
+                    "operands from the calling GPU's own memory only",
+                    name, a.device, dev);
     return FS_OK;
 }
 
@@ -292,6 +359,8 @@ static fs_status run_stage1(int mode, const void *H, const void *W, const Plan &
     CUtensorMap tmH;
     WMaps wm;
     fs_status st;
+    if ((st = require_local_device_memory(H, "H")) != FS_OK) return st;
+    if ((st = require_local_device_memory(W, "W")) != FS_OK) return st;
     // With one batch tile, load only the live rows of H (rounded up to the
     // 8-row swizzle atom); the MMA's other A rows feed TMEM lanes that the
     // epilogue never reads.
@@ -413,6 +482,22 @@ fs_status fs_plan_info(int64_t B, int64_t V, int64_t D, int num_sms, int64_t out
     return FS_OK;
 }
 
+}  // extern "C"
+
+namespace fs {
+size_t sample_workspace_bytes(int64_t B, int64_t V, int64_t D) {
+    if (validate_shape(B, V, D) != FS_OK) return 0;
+    int dev;
+    DeviceInfo info;
+    if (device_info(&dev, &info) != FS_OK) return 0;
+    Plan p;
+    make_plan(B, V, D, info.sms, &p);
+    return p.wsSampleBytes;
+}
+}  // namespace fs
+
+extern "C" {
+
 size_t fs_workspace_size(int64_t B, int64_t V, int64_t D) {
     if (validate_shape(B, V, D) != FS_OK) return 0;
     int dev;
@@ -441,7 +526,7 @@ fs_status fs_stage1(const void *H, const void *W, int64_t B, int64_t V, int64_t 
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
     Plan p;
     make_plan(B, V, D, info.sms, &p);
-    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    if ((st = validate_workspace(workspace, ws_bytes, p.wsSampleBytes)) != FS_OK) return st;
     const Candidates cand = split_workspace(p, workspace);
     const int mode = (flags & FS_FLAG_STORE_LOGITS) ? kModeSampleStore : kModeSample;
     return run_stage1(mode, H, W, p, temperature, temperatures, seed, offset, flags,
@@ -462,7 +547,7 @@ fs_status fs_stage2(int64_t B, int64_t V, int64_t D, float temperature,
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
     Plan p;
     make_plan(B, V, D, info.sms, &p);
-    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    if ((st = validate_workspace(workspace, ws_bytes, p.wsSampleBytes)) != FS_OK) return st;
     const Candidates cand = split_workspace(p, const_cast<void *>(workspace));
     cudaError_t e = launch_stage2(cand.score, cand.idx, p.nCand, B, temperatures, temperature,
                                   out_idx, out_score, static_cast<cudaStream_t>(stream));
@@ -475,8 +560,12 @@ fs_status fs_sample_ex(const void *H, const void *W, int64_t B, int64_t V, int64
                        uint64_t offset, uint32_t flags, int64_t *out_idx, float *out_score,
                        float *out_logits, void *workspace, size_t ws_bytes, void *stream) {
     if (!out_idx) return fail(FS_ERR_INVALID_ARG, "out_idx must be non-null");
-    fs_status st = fs_stage1(H, W, B, V, D, temperature, temperatures, seed, offset, flags,
-                             out_logits, workspace, ws_bytes, stream);
+    // Stage 2's own arguments are checked before Stage 1 launches, so that a
+    // bad output pointer launches nothing.
+    fs_status st = validate_outputs(out_idx, out_score, temperatures);
+    if (st != FS_OK) return st;
+    st = fs_stage1(H, W, B, V, D, temperature, temperatures, seed, offset, flags, out_logits,
+                   workspace, ws_bytes, stream);
     if (st != FS_OK) return st;
     return fs_stage2(B, V, D, temperature, temperatures, out_idx, out_score, workspace, ws_bytes,
                      stream);
@@ -585,6 +674,9 @@ fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V
     int dev;
     DeviceInfo info;
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    // W is checked before the upload of H launches (H's device slot is the
+    // library's own memory).
+    if ((st = require_local_device_memory(W, "W")) != FS_OK) return st;
     Plan p;
     make_plan(B, V, D, info.sms, &p);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -706,7 +798,7 @@ fs_status fs_sample_logprob(const void *H, const void *W, int64_t B, int64_t V, 
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
     Plan p;
     make_plan(B, V, D, info.sms, &p);
-    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    if ((st = validate_workspace(workspace, ws_bytes, p.wsBytes)) != FS_OK) return st;
     const Candidates cand = split_workspace(p, workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = run_stage1(kModeSampleLogprob, H, W, p, temperature, temperatures, seed, offset, 0,
@@ -752,7 +844,9 @@ fs_status fs_sample_transformed(const void *H, const void *W, int64_t B, int64_t
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
     Plan p;
     make_plan(B, V, D, info.sms, &p);
-    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    if ((st = validate_workspace(workspace, ws_bytes, out_logprob ? p.wsBytes : p.wsSampleBytes)) !=
+        FS_OK)
+        return st;
     const Candidates cand = split_workspace(p, workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int mode = out_logprob ? kModeSampleXformLogprob : kModeSampleXform;
@@ -792,7 +886,7 @@ fs_status fs_sample_shard(const void *H, const void *W_shard, int64_t B, int64_t
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
     Plan p;
     make_plan(B, V_shard, D, info.sms, &p);
-    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    if ((st = validate_workspace(workspace, ws_bytes, p.wsBytes)) != FS_OK) return st;
     const Candidates cand = split_workspace(p, workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = run_stage1(kModeSampleLogprob, H, W_shard, p, temperature, temperatures, seed,
@@ -868,7 +962,7 @@ fs_status fs_sample_from_logits(const void *Y, int y_dtype, int64_t B, int64_t V
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
     Plan p;
     make_plan(B, V, 8, info.sms, &p);
-    if ((st = validate_workspace(p, workspace, ws_bytes)) != FS_OK) return st;
+    if ((st = validate_workspace(workspace, ws_bytes, p.wsSampleBytes)) != FS_OK) return st;
     const Candidates cand = split_workspace(p, workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_logits_sample(Y, y_dtype, B, V, temperatures, temperature, seed,

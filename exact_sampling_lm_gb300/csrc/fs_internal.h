@@ -65,10 +65,17 @@ struct Plan {
     int64_t U;     // vocabulary units of 16 rows
     int maxTiles;  // max vocabulary tiles per CTA
     int nChunks;   // blocks per row of the materialised-logits sampler
-    size_t wsBytes;
+    size_t wsBytes;        // all five candidate arrays (log-probability and shard calls)
+    size_t wsSampleBytes;  // the first two (score, index): what plain sampling uses
 };
 
 bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *plan);
+
+// Plan::wsSampleBytes for (B, V, D) on the current device (0 on a bad
+// argument or without a usable device): the candidate bytes that
+// fs_sample_ex, fs_stage1 and fs_stage2 need.
+size_t sample_workspace_bytes(int64_t B, int64_t V, int64_t D);
+
 
 struct Stage1Args {
     int32_t B, V, D;
@@ -107,6 +114,9 @@ cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const WMaps &wm,
                           const Stage1Args &a, int grid,
                           cudaStream_t stream);
 
+// Stage 2 reads Stage 1's device error word (status_word_address): while it
+// is set, every row gets out_idx = -1 and NaN scores, so a call whose Stage 1
+// gave up a bounded wait never returns tokens from a partial candidate buffer.
 cudaError_t launch_stage2(const float *cand_score, const int32_t *cand_idx, int nCand,
                           int64_t B, const float *temps, float temp_scalar, int64_t *out_idx,
                           float *out_score, cudaStream_t stream);
@@ -139,5 +149,14 @@ cudaError_t launch_debug_noise(uint64_t seed, uint64_t offset, int64_t b0, int64
 
 // Device error word of Stage 1 (bit 0: a bounded wait expired).
 cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *word);
+
+// Device address of that word in the current CUDA context, for the kernels of
+// other translation units (looked up once per context, then cached).
+cudaError_t status_word_address(uint32_t **out);
+
+// Identifier of the CUDA context current on this thread (unique for the life
+// of the process, unlike a context handle, which a destroyed context may pass
+// on); false when no context is current or the driver lacks the query.
+bool current_context_id(unsigned long long *id);
 
 }  // namespace fs

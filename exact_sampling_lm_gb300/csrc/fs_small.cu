@@ -50,7 +50,8 @@ constexpr int kStage2Warps = 8;
 __global__ void __launch_bounds__(kStage2Warps * 32)
     stage2_kernel(const float *__restrict__ cand_score, const int32_t *__restrict__ cand_idx,
                   int nCand, int64_t B, const float *__restrict__ temps, float temp_scalar,
-                  int64_t *__restrict__ out_idx, float *__restrict__ out_score) {
+                  int64_t *__restrict__ out_idx, float *__restrict__ out_score,
+                  const uint32_t *__restrict__ status) {
     // The next kernel of the stream (the next call's Stage 1) may launch now:
     // it only sets itself up before waiting for this grid.  Launched with
     // programmatic serialization itself: wait for the producing grid.
@@ -59,6 +60,14 @@ __global__ void __launch_bounds__(kStage2Warps * 32)
     const int lane = threadIdx.x & 31;
     const int64_t b = static_cast<int64_t>(blockIdx.x) * kStage2Warps + (threadIdx.x >> 5);
     if (b >= B) return;
+    if (*status != 0u) {
+        // a Stage 1 gave up a bounded wait: its candidates are incomplete
+        if (lane == 0) {
+            out_idx[b] = -1;
+            if (out_score) out_score[b] = __int_as_float(0x7fc00000);
+        }
+        return;
+    }
     float best = -INFINITY;
     uint32_t bi = 0xFFFFFFFFu;
     for (int i = lane; i < nCand; i += 32) {
@@ -94,8 +103,11 @@ cudaError_t launch_stage2(const float *cand_score, const int32_t *cand_idx, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    uint32_t *status = nullptr;
+    cudaError_t e = status_word_address(&status);
+    if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, stage2_kernel, cand_score, cand_idx, nCand, B, temps,
-                              temp_scalar, out_idx, out_score);
+                              temp_scalar, out_idx, out_score, static_cast<const uint32_t *>(status));
 }
 
 // ------------------------------------------------------------------ host-buffer upload
@@ -163,12 +175,22 @@ __global__ void __launch_bounds__(kStage2Warps * 32)
                           int nCand, int64_t B, const float *__restrict__ temps,
                           float temp_scalar, int64_t *__restrict__ out_idx,
                           float *__restrict__ out_score, float *__restrict__ out_logprob,
-                          float *__restrict__ out_logmass) {
+                          float *__restrict__ out_logmass, const uint32_t *__restrict__ status) {
     griddep_launch_dependents();  // as in stage2_kernel
     griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t b = static_cast<int64_t>(blockIdx.x) * kStage2Warps + (threadIdx.x >> 5);
     if (b >= B) return;
+    if (*status != 0u) {  // as in stage2_kernel
+        if (lane == 0) {
+            const float nan = __int_as_float(0x7fc00000);
+            out_idx[b] = -1;
+            if (out_score) out_score[b] = nan;
+            if (out_logprob) out_logprob[b] = nan;
+            if (out_logmass) out_logmass[b] = nan;
+        }
+        return;
+    }
     float best = -INFINITY, blt = __int_as_float(0x7fc00000);
     uint32_t bi = 0xFFFFFFFFu;
     float m = -INFINITY, sum = 0.0f;
@@ -228,9 +250,12 @@ cudaError_t launch_stage2_logprob(const float *cand_score, const int32_t *cand_i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    uint32_t *status = nullptr;
+    cudaError_t e = status_word_address(&status);
+    if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, stage2_logprob_kernel, cand_score, cand_idx, cand_lt, cand_m,
                               cand_s, nCand, B, temps, temp_scalar, out_idx, out_score,
-                              out_logprob, out_logmass);
+                              out_logprob, out_logmass, static_cast<const uint32_t *>(status));
 }
 
 // ------------------------------------------------------------------ grouped sampler

@@ -51,6 +51,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <map>
 #include <mutex>
 
 #include "fs_internal.h"
@@ -900,6 +901,30 @@ cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const WMaps &wm,
             return launch_mode<kModeSampleXformLogprob, 1>(tmH, wm, a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t status_word_address(uint32_t **out) {
+    // A context that is destroyed and created again (cudaDeviceReset) loads
+    // the module anew, so the cache is keyed by context, not by device.
+    static std::mutex mu;
+    static std::map<unsigned long long, uint32_t *> by_context;
+    unsigned long long ctx = 0;
+    bool have_ctx = current_context_id(&ctx);
+    std::lock_guard<std::mutex> lock(mu);
+    if (have_ctx) {
+        auto it = by_context.find(ctx);
+        if (it != by_context.end()) {
+            *out = it->second;
+            return cudaSuccess;
+        }
+    }
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return e;
+    // the lookup itself makes the device's primary context current if none was
+    if (have_ctx || current_context_id(&ctx)) by_context[ctx] = static_cast<uint32_t *>(p);
+    *out = static_cast<uint32_t *>(p);
+    return cudaSuccess;
 }
 
 cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *word) {

@@ -24,6 +24,13 @@
  *   - H and W must be 16-byte aligned and D must be a multiple of 8 (the
  *     tensor-memory-access unit needs 16-byte rows); otherwise the call
  *     returns FS_ERR_UNSUPPORTED and launches nothing.
+ *   - H and W must be device memory of the current GPU (cudaMalloc-family or
+ *     pool memory of that device).  Stage 1 reads them with tensor-memory
+ *     loads, and its paired form (two CTAs of a cluster sharing each W tile)
+ *     multicasts every W box into both CTAs; those loads are kept to the
+ *     calling GPU's own memory.  Page-locked host memory, another GPU's
+ *     memory (peer access) and managed memory are refused with
+ *     FS_ERR_UNSUPPORTED before anything is launched.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are asynchronous on `stream`: a returned FS_OK means the
  *     work was enqueued; device-side errors surface at the caller's next
@@ -145,8 +152,12 @@ fs_status fs_sample_host(const void *H_host, const void *W, int64_t B, int64_t V
                          uint64_t offset, int64_t *out_idx_host, float *out_score_host,
                          void *stream);
 
-/* Bytes of caller workspace that fs_sample_ex, fs_stage1/fs_stage2 and
- * fs_sample_from_logits need for (B, V, D) on the current device.
+/* Bytes of caller workspace for (B, V, D) on the current device: enough for
+ * every entry point that takes a workspace.  It holds five equal candidate
+ * arrays; the calls that sample without a log-probability (fs_sample_ex,
+ * fs_stage1/fs_stage2, fs_sample_from_logits, fs_sample_unfused and
+ * fs_sample_transformed without out_logprob) use only the first two and
+ * accept any ws_bytes >= 2/5 of this size.
  * Returns 0 on a bad argument or when no device is visible. */
 size_t fs_workspace_size(int64_t B, int64_t V, int64_t D);
 
@@ -321,6 +332,10 @@ fs_status fs_debug_gumbel(const uint32_t *words, int64_t n, float *out_g, void *
  * NULL) receives the raw bits: 1 = a bounded wait inside a kernel expired.
  * Returns FS_ERR_TIMEOUT if any bit was set, FS_ERR_CUDA if a CUDA call
  * failed, FS_OK otherwise.
+ * While the word is set, every Stage 2 (of any sampling entry point) writes
+ * out_idx = -1 and NaN to out_score / out_logprob / out_logmass for every
+ * row instead of reducing candidates, so a call whose Stage 1 gave up never
+ * returns tokens; clearing the word here restores normal results.
  * ------------------------------------------------------------------------- */
 fs_status fs_get_device_status(void *stream, uint32_t *out_word);
 
@@ -343,9 +358,12 @@ fs_status fs_plan_info(int64_t B, int64_t V, int64_t D, int num_sms, int64_t out
  * Arguments, results and errors are those of fs_sample.  The candidate
  * scratch is a static array of FS_NOALLOC_SCRATCH_BYTES inside the library's
  * device memory (held on every GPU that loads the library until the process
- * exits); a call whose candidates need more (fs_workspace_size(B, V, D) >
- * FS_NOALLOC_SCRATCH_BYTES) returns FS_ERR_UNSUPPORTED and launches nothing.
- * The first call on each device looks up the array's device address
+ * exits).  A call keeps two candidate arrays (score, index) of
+ * max(partitions, ceil(V / 8192)) x B four-byte values each, rounded up to
+ * 256 bytes (partitions = floor(SMs / ceil(B / 128)), at least 1); a call
+ * that needs more than the array returns FS_ERR_UNSUPPORTED and launches
+ * nothing (on a 152-SM GPU every B up to 8192 fits at V = 128256).
+ * The first call in each CUDA context looks up the array's device address
  * (cudaGetSymbolAddress), so make that first call before any stream capture.
  * All calls share the array: calls whose kernels overlap on the GPU (other
  * streams, other host threads) race on it and must be serialised by the

@@ -195,6 +195,20 @@ def test_misaligned_outputs_are_rejected():
         _lib.FS_ERR_UNSUPPORTED
 
 
+def test_sample_ex_checks_outputs_before_stage1():
+    """fs_sample_ex checks Stage 2's outputs before Stage 1 launches: a
+    misaligned out_score or out_idx is refused before any device call (on a
+    machine without a GPU the status is the validation error, not a CUDA
+    error from the device query)."""
+    L = _lib.lib()
+    ws = 1 << 20
+    assert L.fs_sample_ex(16, 16, 4, 64, 64, 1.0, None, 0, 0, 0, 16, 18, None, 32, ws, None) == \
+        _lib.FS_ERR_UNSUPPORTED
+    assert L.fs_sample_ex(16, 16, 4, 64, 64, 1.0, None, 0, 0, 0, 20, None, None, 32, ws, None) == \
+        _lib.FS_ERR_UNSUPPORTED
+    assert "aligned" in fs.fs_last_error_string()
+
+
 def test_binding_checks_per_row_temperature_length():
     from exact_sampling_lm_gb300 import _lib as b
     with pytest.raises(b.FSError):

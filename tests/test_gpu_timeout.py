@@ -4,8 +4,9 @@ Every mbarrier wait in Stage 1 gives up after FS_WAIT_TIMEOUT_MS; the CTA
 then sets the library's device error word, tells its other warps to stop,
 frees its tensor memory and returns.  The test hook FS_FLAG_TEST_NO_LOADS
 makes the loader issue nothing, so the first wait of every CTA runs out; the
-host must read FS_ERR_TIMEOUT, and the context must stay usable (a normal call
-afterwards still matches the oracle's sample).  Runs in a child process so that
+call's Stage 2 must then return no token (index -1, NaN score) for every row,
+the host must read FS_ERR_TIMEOUT, and the context must stay usable (once the
+word is cleared, normal calls agree again).  Runs in a child process so that
 the short timeout applies only there.
 """
 import os
@@ -31,9 +32,18 @@ for B, V, D in ((4, 4096, 256), (256, 20000, 64)):  # unpaired and 2-CTA-cluster
     W = (torch.randn((V, D), generator=g) * 0.1).to(torch.bfloat16).cuda()
     ws = fs.workspace(B, V, D)
     t0 = time.time()
+    # the whole call: Stage 1 gives up, and Stage 2 returns no token
+    idx, score, _ = fs.fs_sample_ex(H, W, temperature=1.0, seed=1, offset=0, flags=0x100, ws=ws)
+    torch.cuda.synchronize()
+    dt = time.time() - t0
+    assert torch.all(idx == -1) and torch.all(torch.isnan(score)), idx
+    # while the word is set, every later Stage 2 refuses too (log-probability
+    # form included), whatever its candidates hold
+    i2, s2, lp = fs.fs_sample_logprob(H, W, temperature=1.0, seed=1, offset=0)
+    torch.cuda.synchronize()
+    assert torch.all(i2 == -1) and torch.all(torch.isnan(s2)) and torch.all(torch.isnan(lp))
     fs.fs_stage1(H, W, ws, temperature=1.0, seed=1, offset=0, flags=0x100)
     word = fs.fs_get_device_status()
-    dt = time.time() - t0
     assert word == 1, word
     assert 0.1 < dt < 30, dt
     # the context still works and the word was cleared

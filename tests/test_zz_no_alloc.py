@@ -66,10 +66,35 @@ def test_noalloc_matches_fs_sample_on_two_calls(fs, B, V, D, T):
     assert fs.fs_get_device_status() == 0
 
 
+def sample_scratch_bytes(B, V):
+    """The two candidate arrays (score, index) plain sampling keeps: each
+    max(partitions, ceil(V / 8192)) x B four-byte values, rounded to 256 B."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    parts = max(1, min(sms // ((B + 127) // 128), (V + 15) // 16))
+    slots = max(parts, (V + 8191) // 8192)
+    return 2 * ((slots * B * 4 + 255) // 256 * 256)
+
+
+def test_noalloc_takes_what_only_the_two_sampling_arrays_fit(fs):
+    """B = 4096 at V = 128256: the full workspace (five arrays, for the
+    log-probability calls) exceeds the scratch, the two arrays that sampling
+    keeps do not; the call is accepted and agrees with fs_sample."""
+    B, V, D = 4096, 128256, 64
+    assert fs.fs_workspace_size(B, V, D) > SCRATCH_BYTES >= sample_scratch_bytes(B, V)
+    g = torch.Generator(device="cpu").manual_seed(77)
+    dev = torch.device("cuda:0")
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * 0.1).to(torch.bfloat16).to(dev)
+    for offset in (3, 4):
+        a_idx, a_score = noalloc_call(fs, H, W, 0.9, 99, offset)
+        b_idx, b_score = fs.fs_sample(H, W, temperature=0.9, seed=99, offset=offset)
+        torch.cuda.synchronize()
+        assert torch.equal(a_idx, b_idx) and torch.equal(a_score, b_score)
+
+
 def test_noalloc_refuses_requests_beyond_its_scratch(fs):
     B, V, D = 8192, 262144, 8
-    need = fs.fs_workspace_size(B, V, D)
-    assert need > SCRATCH_BYTES
+    assert sample_scratch_bytes(B, V) > SCRATCH_BYTES
     dev = torch.device("cuda:0")
     H = torch.zeros((B, D), dtype=torch.bfloat16, device=dev)
     W = torch.zeros((V, D), dtype=torch.bfloat16, device=dev)
