@@ -17,8 +17,10 @@
  *  - l~ = l / T, the one deterministic transform applied before the noise.
  *
  * Readings where the pages are silent (each one is listed in the design notes):
- *  - logits: exact products of bf16 values summed in fp64 in index order
- *    k = 0..D-1, then rounded once to f32 (the GPU accumulates in f32);
+ *  - logits: bf16 inputs with f32 accumulation (the experimental setup's
+ *    precision): each product of two bf16 values is exact in f32, and the
+ *    sum runs in f32 in index order k = 0..D-1, rounded after every addition.
+ *    An fp64 sum of the same products is kept for diagnostics only;
  *  - temperature: invT = 1.0f / T in f32, l~ = l * invT in f32; rows whose T is
  *    not finite or not > 0 get index -1 and score NaN (greedy is not part of the
  *    method, Section 5 GSM8K paragraph);
@@ -142,24 +144,37 @@ void oracle_gumbel_block(const uint32_t *x, int64_t n, float *g, int nthreads) {
 /* ---------------------------------------------------------------------------
  * LM-head logits l[b, v] = sum_k H[b, k] * W[v, k].
  * H is [B, D] and W is [V, D], both row-major bf16 given as raw 16-bit words.
- * bf16 -> double is exact and so is each product; the sum runs in fp64 in
- * index order.
+ * bf16 -> f32 is exact, and so is the f32 product of two bf16 values (8 + 8
+ * significant bits fit in 24).  The sum runs in f32 in index order
+ * k = 0..D-1 and is rounded to f32 after every addition; -ffp-contract=off
+ * keeps each product and addition apart (no fused multiply-add).
  * ------------------------------------------------------------------------- */
-static double bf16_to_double(uint16_t h) {
+static float bf16_to_float(uint16_t h) {
     uint32_t bits = (uint32_t)h << 16;
     float f;
     memcpy(&f, &bits, sizeof f);
-    return (double)f;
+    return f;
 }
 
-static double dot_row(const uint16_t *h, const uint16_t *w, int64_t D) {
+static float dot_row(const uint16_t *h, const uint16_t *w, int64_t D) {
+    float acc = 0.0f;
+    for (int64_t k = 0; k < D; ++k) {
+        float p = bf16_to_float(h[k]) * bf16_to_float(w[k]);
+        acc = acc + p;
+    }
+    return acc;
+}
+
+/* Diagnostic only: the same exact products summed in fp64 in index order. */
+static double dot_row64(const uint16_t *h, const uint16_t *w, int64_t D) {
     double acc = 0.0;
-    for (int64_t k = 0; k < D; ++k) acc += bf16_to_double(h[k]) * bf16_to_double(w[k]);
+    for (int64_t k = 0; k < D; ++k)
+        acc += (double)bf16_to_float(h[k]) * (double)bf16_to_float(w[k]);
     return acc;
 }
 
 void oracle_logits(const uint16_t *H, const uint16_t *W, int64_t B, int64_t V,
-                   int64_t D, double *out, int nthreads) {
+                   int64_t D, float *out, int nthreads) {
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #endif
@@ -167,6 +182,18 @@ void oracle_logits(const uint16_t *H, const uint16_t *W, int64_t B, int64_t V,
     for (int64_t i = 0; i < B * V; ++i) {
         int64_t b = i / V, v = i % V;
         out[i] = dot_row(H + b * D, W + v * D, D);
+    }
+}
+
+void oracle_logits64(const uint16_t *H, const uint16_t *W, int64_t B, int64_t V,
+                     int64_t D, double *out, int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < B * V; ++i) {
+        int64_t b = i / V, v = i % V;
+        out[i] = dot_row64(H + b * D, W + v * D, D);
     }
 }
 
@@ -244,33 +271,28 @@ void oracle_sample_from_logits(const float *logits, int64_t B, int64_t V,
     free(s);
 }
 
-/* The whole hot path from H and W: logits (fp64 sum rounded to f32), then the
- * full Gumbel-max pass.  row_ids as for oracle_sample_from_logits.
- * out_logits [B, V] (fp64, optional) receives the unrounded sums for
- * logits-tolerance checks. */
+/* The whole hot path from H and W: the f32 logits, then the full Gumbel-max
+ * pass.  row_ids as for oracle_sample_from_logits.  out_logits [B, V] (f32,
+ * optional) receives the logits the pass sampled from, for the logits
+ * tolerance checks. */
 void oracle_sample(const uint16_t *H, const uint16_t *W, int64_t B, int64_t V,
                    int64_t D, const float *T, const int64_t *row_ids, uint64_t seed,
                    uint64_t offset, uint32_t flags, int64_t *out_idx, float *out_score,
-                   float *out_second, double *out_logits, int nthreads) {
+                   float *out_second, float *out_logits, int nthreads) {
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #endif
-    double *l64 = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
     float *l32 = (float *)malloc(sizeof(float) * (size_t)(V > 0 ? V : 1));
     float *s = (float *)malloc(sizeof(float) * (size_t)(V > 0 ? V : 1));
     for (int64_t b = 0; b < B; ++b) {
         const uint16_t *h = H + b * D;
         #pragma omp parallel for schedule(static)
-        for (int64_t v = 0; v < V; ++v) {
-            l64[v] = dot_row(h, W + v * D, D);
-            l32[v] = (float)l64[v];
-        }
-        if (out_logits) memcpy(out_logits + b * V, l64, sizeof(double) * (size_t)V);
+        for (int64_t v = 0; v < V; ++v) l32[v] = dot_row(h, W + v * D, D);
+        if (out_logits) memcpy(out_logits + b * V, l32, sizeof(float) * (size_t)V);
         int64_t row = row_ids ? row_ids[b] : b;
         sample_row(l32, row, V, T[b], seed, offset, flags, s, &out_idx[b],
                    &out_score[b], &out_second[b]);
     }
-    free(l64);
     free(l32);
     free(s);
 }
@@ -387,7 +409,7 @@ void oracle_sample_shard(const uint16_t *H, const uint16_t *W_shard, int64_t B, 
         float invT = 1.0f / Tb;
         const uint16_t *h = H + b * D;
         #pragma omp parallel for schedule(static)
-        for (int64_t v = 0; v < Vs; ++v) lt[v] = (float)dot_row(h, W_shard + v * D, D) * invT;
+        for (int64_t v = 0; v < Vs; ++v) lt[v] = dot_row(h, W_shard + v * D, D) * invT;
         float best = -INFINITY, second = -INFINITY;
         int64_t bi = -1;
         double mx = -INFINITY;

@@ -46,6 +46,8 @@ def _load():
         lib.oracle_gumbel_block.restype = None
         lib.oracle_logits.argtypes = [vp, vp, i64, i64, i64, vp, i32]
         lib.oracle_logits.restype = None
+        lib.oracle_logits64.argtypes = [vp, vp, i64, i64, i64, vp, i32]
+        lib.oracle_logits64.restype = None
         lib.oracle_sample_from_logits.argtypes = [vp, i64, i64, vp, vp, u64, u64, u32,
                                                   vp, vp, vp, vp, i32]
         lib.oracle_sample_from_logits.restype = None
@@ -133,14 +135,27 @@ def noise_block(seed, offset, b0, nb, v0, nv, nthreads=0):
 
 
 def logits(H_bits, W_bits, nthreads=0):
-    """fp64 logits H W^T from raw bf16 words H [B, D] and W [V, D]."""
+    """The oracle's logits H W^T (f32 [B, V]) from raw bf16 words H [B, D] and
+    W [V, D]: exact f32 products summed in f32 in index order k = 0..D-1."""
+    H = _c(H_bits, np.uint16)
+    W = _c(W_bits, np.uint16)
+    B, D = H.shape
+    V, D2 = W.shape
+    assert D == D2
+    out = np.zeros((B, V), dtype=np.float32)
+    _load().oracle_logits(_ptr(H), _ptr(W), B, V, D, _ptr(out), nthreads)
+    return out
+
+
+def logits64(H_bits, W_bits, nthreads=0):
+    """Diagnostic: the same products summed in fp64 (float64 [B, V])."""
     H = _c(H_bits, np.uint16)
     W = _c(W_bits, np.uint16)
     B, D = H.shape
     V, D2 = W.shape
     assert D == D2
     out = np.zeros((B, V), dtype=np.float64)
-    _load().oracle_logits(_ptr(H), _ptr(W), B, V, D, _ptr(out), nthreads)
+    _load().oracle_logits64(_ptr(H), _ptr(W), B, V, D, _ptr(out), nthreads)
     return out
 
 
@@ -187,7 +202,8 @@ def sample(H_bits, W_bits, T, seed, offset, flags=0, want_logits=False, nthreads
     """The whole path from bf16 H [B, D] and W [V, D].
 
     row_ids: optional row index (in the full batch) of each given row of H.
-    Returns (idx int64 [B], best f32 [B], second f32 [B], logits64 or None).
+    Returns (idx int64 [B], best f32 [B], second f32 [B], logits or None),
+    the logits being the f32 [B, V] the pass sampled from.
     """
     H = _c(H_bits, np.uint16)
     W = _c(W_bits, np.uint16)
@@ -199,10 +215,10 @@ def sample(H_bits, W_bits, T, seed, offset, flags=0, want_logits=False, nthreads
     idx = np.zeros(B, dtype=np.int64)
     best = np.zeros(B, dtype=np.float32)
     second = np.zeros(B, dtype=np.float32)
-    l64 = np.zeros((B, V), dtype=np.float64) if want_logits else None
+    l32 = np.zeros((B, V), dtype=np.float32) if want_logits else None
     _load().oracle_sample(_ptr(H), _ptr(W), B, V, D, _ptr(Tv), _ptr(rows), seed, offset, flags,
-                          _ptr(idx), _ptr(best), _ptr(second), _ptr(l64), nthreads)
-    return idx, best, second, l64
+                          _ptr(idx), _ptr(best), _ptr(second), _ptr(l32), nthreads)
+    return idx, best, second, l32
 
 
 def group_gumbel(seed, offset, b, g) -> float:
@@ -273,4 +289,4 @@ def logprob(l32, T, idx):
 
 __all__ = ["group_gumbel", "sample_shard", "combine_groups", "transform_logits", "logprob", "NO_NOISE", "num_threads", "philox4x64_10", "noise_word", "uniform",
            "gumbel_from_word", "gumbel", "uniform_block", "gumbel_block", "noise_block", "logits",
-           "sample_from_logits", "sample"]
+           "logits64", "sample_from_logits", "sample"]

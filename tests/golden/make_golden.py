@@ -51,11 +51,11 @@ def extra_inputs(B, V):
 
 def compute():
     H, W, T, seed, offset = tiny_inputs()
-    idx, best, second, l64 = oracle.sample(H, W, T, seed, offset, want_logits=True)
+    idx, best, second, l32 = oracle.sample(H, W, T, seed, offset, want_logits=True)
     idx1, best1, second1, _ = oracle.sample(H, W, T, seed, offset + 1)
     # the wider rows: log-probability of the sample, transforms, shards and
     # the grouped combine, on the same inputs
-    l32 = oracle.logits(H, W).astype(np.float32)
+    assert np.array_equal(l32, oracle.logits(H, W))
     lp = oracle.logprob(l32, T, idx)
     bias, mask = extra_inputs(*l32.shape)
     lx = oracle.transform_logits(l32, bias=bias, softcap=15.0, mask=mask)
@@ -72,8 +72,8 @@ def compute():
         "idx": [idx.tolist(), idx1.tolist()],
         "best": [[float(x) for x in best], [float(x) for x in best1]],
         "second": [[float(x) for x in second], [float(x) for x in second1]],
-        "logits_row0_first8": [float(x) for x in l64[0, :8]],
-        "logits_sum": float(np.sum(l64)),
+        "logits_row0_first8": [float(x) for x in l32[0, :8]],
+        "logits_sum": float(np.sum(l32.astype(np.float64))),
         "logprob": [float(x) for x in lp],
         "xform_idx": xidx.tolist(),
         "xform_best": [float(x) for x in xbest],

@@ -3,10 +3,14 @@
 FlashSampling (arXiv 2603.15854) fixes the result as the maximizer of the
 perturbed logits s_i = l~_i + g_i over the whole vocabulary (method section;
 exactness by Appendix C: argmax decomposes over a partition), which is an exact
-sample from softmax(l~) with l~ = l / T.  The checks below pin the oracle to
-things outside itself: a numpy fp64 matmul, exact integer arithmetic, brute
-force on tiny vocabularies, partition invariance, the softmax law by
-chi-squared tests and quadrature, and the temperature's placement.
+sample from softmax(l~) with l~ = l / T.  The logits are bf16 products
+accumulated in f32 (the experimental setup's precision), summed in index
+order.  The checks below pin the oracle to things outside itself: a
+sequential float32 sum written with numpy, the textbook error bound of that
+sum against an exact one, a numpy fp64 matmul for the diagnostic sums, exact
+integer arithmetic, brute force on tiny vocabularies, partition invariance,
+the softmax law by chi-squared tests and quadrature, and the temperature's
+placement.
 """
 import math
 
@@ -31,12 +35,63 @@ def bits_to_f64(bits):
 
 # ---------------------------------------------------------------- logits
 
-@pytest.mark.parametrize("B,V,D", [(3, 50, 1), (2, 33, 7), (5, 129, 64), (4, 300, 257)])
-def test_logits_match_numpy_fp64_matmul(B, V, D):
+def sequential_f32_sum(Hf32, Wf32):
+    """l[b, v] = sum_k H[b, k] W[v, k] with numpy float32: every product and
+    every partial sum rounded to float32, k from 0 to D-1 (an independent
+    statement of the accumulation the oracle's logits are defined by)."""
+    B, D = Hf32.shape
+    acc = np.zeros((B, Wf32.shape[0]), dtype=np.float32)
+    for k in range(D):
+        prod = (Hf32[:, k:k + 1] * Wf32[None, :, k]).astype(np.float32)
+        acc = (acc + prod).astype(np.float32)
+    return acc
+
+
+@pytest.mark.parametrize("B,V,D", [(3, 50, 1), (2, 33, 7), (5, 129, 64), (4, 300, 257),
+                                   (2, 64, 1031)])
+def test_logits_equal_a_sequential_float32_sum(B, V, D):
+    """Bit for bit: the oracle's logits are the f32 sum in index order.  An
+    fp64 sum rounded once, another summation order (reversed, two halves) or
+    a dropped term each change some of these last bits.  A fused
+    multiply-add would not: a bf16 x bf16 product is exact in f32, so
+    fma(h, w, acc) and acc + h * w round the same exact value."""
     rng = np.random.default_rng(B * 1000 + D)
     H = bf16_bits(rng.standard_normal((B, D)))
     W = bf16_bits(0.05 * rng.standard_normal((V, D)))
     got = oracle.logits(H, W)
+    assert got.dtype == np.float32
+    want = sequential_f32_sum(bits_to_f64(H).astype(np.float32), bits_to_f64(W).astype(np.float32))
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("D", [64, 1000, 4096])
+def test_logits_within_the_textbook_bound_of_the_exact_sum(D):
+    """A recursive f32 sum of exact products errs by at most
+    gamma_(D-1) * sum_k |h_k w_k|, gamma_n = n u / (1 - n u), u = 2^-24
+    (Higham, Accuracy and Stability of Numerical Algorithms, recursive
+    summation).  The exact sum comes from Python fractions."""
+    from fractions import Fraction
+    rng = np.random.default_rng(D)
+    B, V = 2, 6
+    H = bf16_bits(rng.standard_normal((B, D)))
+    W = bf16_bits(0.02 * rng.standard_normal((V, D)))
+    got = oracle.logits(H, W)
+    Hf, Wf = bits_to_f64(H), bits_to_f64(W)
+    u = 2.0 ** -24
+    gamma = (D - 1) * u / (1 - (D - 1) * u)
+    for b in range(B):
+        for v in range(V):
+            exact = sum(Fraction(float(Hf[b, k])) * Fraction(float(Wf[v, k])) for k in range(D))
+            bound = gamma * float(np.sum(np.abs(Hf[b] * Wf[v])))
+            assert abs(Fraction(float(got[b, v])) - exact) <= Fraction(bound)
+
+
+@pytest.mark.parametrize("B,V,D", [(3, 50, 1), (2, 33, 7), (5, 129, 64), (4, 300, 257)])
+def test_diagnostic_fp64_logits_match_numpy_matmul(B, V, D):
+    rng = np.random.default_rng(B * 1000 + D)
+    H = bf16_bits(rng.standard_normal((B, D)))
+    W = bf16_bits(0.05 * rng.standard_normal((V, D)))
+    got = oracle.logits64(H, W)
     Hf, Wf = bits_to_f64(H), bits_to_f64(W)
     want = Hf @ Wf.T
     scale = np.abs(Hf) @ np.abs(Wf).T
@@ -44,30 +99,33 @@ def test_logits_match_numpy_fp64_matmul(B, V, D):
 
 
 def test_logits_exact_on_small_integers():
-    """Small integers are exact in bf16; the sums are exact integers."""
+    """Small integers are exact in bf16, and every partial sum here stays an
+    integer below 2^24, so both sums are the exact integers."""
     rng = np.random.default_rng(3)
     B, V, D = 3, 17, 45
     Hi = rng.integers(-8, 9, size=(B, D))
     Wi = rng.integers(-8, 9, size=(V, D))
     got = oracle.logits(bf16_bits(Hi), bf16_bits(Wi))
+    got64 = oracle.logits64(bf16_bits(Hi), bf16_bits(Wi))
     for b in range(B):
         for v in range(V):
             want = sum(int(Hi[b, k]) * int(Wi[v, k]) for k in range(D))
-            assert got[b, v] == want
+            assert got[b, v] == want and got64[b, v] == want
 
 
-def test_sample_uses_f32_rounded_logits():
-    """oracle.sample == oracle.sample_from_logits on f32(logits)."""
+def test_sample_uses_the_f32_logits():
+    """oracle.sample == oracle.sample_from_logits on the oracle's f32 logits,
+    and the logits it returns are those."""
     rng = np.random.default_rng(11)
     B, V, D = 6, 200, 96
     H = bf16_bits(rng.standard_normal((B, D)))
     W = bf16_bits(0.1 * rng.standard_normal((V, D)))
     T = np.array([1.0, 0.5, 1.5, 0.7, 2.0, 1.0], dtype=np.float32)
-    i1, s1, t1, l64 = oracle.sample(H, W, T, 42, 9, want_logits=True)
-    i2, s2, t2, _ = oracle.sample_from_logits(l64.astype(np.float32), T, 42, 9)
+    i1, s1, t1, l32 = oracle.sample(H, W, T, 42, 9, want_logits=True)
+    i2, s2, t2, _ = oracle.sample_from_logits(l32, T, 42, 9)
     assert np.array_equal(i1, i2)
     assert np.array_equal(s1, s2) and np.array_equal(t1, t2)
-    assert np.array_equal(l64, oracle.logits(H, W))
+    assert np.array_equal(l32, oracle.logits(H, W))
 
 
 # ---------------------------------------------------------------- argmax
@@ -354,7 +412,7 @@ def test_one_group_is_the_plain_sample():
     out, grp = oracle.combine_groups(i1[None, :], lm1[None, :], 8, 2)
     assert np.array_equal(out, idx_full) and np.all(grp == 0)
     # a shard's log-mass is scipy's logsumexp of its l~
-    l32 = oracle.logits(H, W).astype(np.float32)
+    l32 = oracle.logits(H, W)
     i2, s2, lm2, _ = oracle.sample_shard(H, W[32:80], 32, T, 8, 2)
     for b in range(B):
         lt = (l32[b, 32:80] * (np.float32(1) / T[b])).astype(np.float64)
