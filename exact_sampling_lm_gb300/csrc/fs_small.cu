@@ -308,7 +308,13 @@ cudaError_t launch_combine_groups(int64_t n_groups, int64_t B, const int64_t *gr
 
 // ------------------------------------------------------------------ unfused sampling pass
 // Block (chunk, row): 256 threads scan kLogitsChunk logits of one row, 8 per
-// thread per step (one Philox call), then reduce to one candidate.
+// thread per step (one Philox call), then reduce to one candidate.  Like the
+// Stage 1 epilogue, each step screens its 8 elements against the thread's
+// best before the step (screen_lg2_tail / screen_bound) and pays for the
+// exact Gumbel only for the survivors, lowest index first; the screen is
+// conservative, so the result equals scoring every element.  The fused and
+// unfused paths then differ only by the logits' write and read-back, the
+// traffic the IO model counts.
 template <typename T>
 __device__ __forceinline__ void load8(const T *row, int64_t v, int64_t v_end, bool vec_ok,
                                       float (&l)[8]);
@@ -369,13 +375,40 @@ __global__ void __launch_bounds__(kLogitsThreads)
             for (int64_t v = v_begin + threadIdx.x * 8; v < v_end; v += kLogitsThreads * 8) {
                 float l[8];
                 load8<T>(row, v, v_end, vec_ok, l);
-                uint32_t x[8];
-                if (!no_noise) noise_words8(prow, static_cast<uint64_t>(v) >> 3, x);
+                if (no_noise) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float g = no_noise ? 0.0f : gumbel_from_word(x[e]);
-                    const float s = __fadd_rn(__fmul_rn(l[e], invT), g);
-                    if (v + e < v_end && s > best) {
+                    for (int e = 0; e < 8; ++e) {
+                        const float s = __fmul_rn(l[e], invT);
+                        if (v + e < v_end && s > best) {
+                            best = s;
+                            bi = static_cast<uint32_t>(v + e);
+                        }
+                    }
+                    continue;
+                }
+                uint32_t x[8];
+                noise_words8(prow, static_cast<uint64_t>(v) >> 3, x);
+                float lt[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) lt[e] = __fmul_rn(l[e], invT);
+                const float best0 = best;
+                uint32_t pass = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (v + e < v_end && screen_lg2_tail(x[e]) < screen_bound(lt[e], best0))
+                        pass |= 1u << e;
+                while (pass) {
+                    const int e = __ffs(pass) - 1;
+                    pass &= pass - 1;
+                    float lte = lt[0];
+                    uint32_t xe = x[0];
+#pragma unroll
+                    for (int k = 1; k < 8; ++k) {
+                        lte = (e == k) ? lt[k] : lte;
+                        xe = (e == k) ? x[k] : xe;
+                    }
+                    const float s = __fadd_rn(lte, gumbel_from_word(xe));
+                    if (s > best) {
                         best = s;
                         bi = static_cast<uint32_t>(v + e);
                     }
