@@ -116,18 +116,17 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
-// Same load, delivered to the same shared-memory offset (data and mbarrier
-// completion) of every CTA of the cluster named in cta_mask.  Used only
-// between CTAs of one cluster on this GPU.
-__device__ __forceinline__ void tma_load_2d_multicast(void *smem_dst, const CUtensorMap *map,
-                                                      uint64_t *bar, int32_t x, int32_t y,
-                                                      uint16_t cta_mask, uint64_t policy) {
+// Pair form (.cta_group::2): the box lands in this CTA's shared memory, and
+// its bytes complete on the mbarrier at shared::cluster address bar_cluster,
+// which may belong to either CTA of this CTA's pair (used to signal the pair
+// leader's barrier from the peer).
+__device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y,
+                                                 uint64_t policy) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(
-            smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask),
-        "l"(policy)
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
         : "memory");
 }
 
@@ -144,6 +143,51 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
+}
+
+// The shared::cluster address of the variable at CTA-local shared address
+// `addr` in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive (once) on an mbarrier of another CTA of the cluster, given by its
+// shared::cluster address; release at cluster scope orders this thread's
+// earlier memory accesses (and what it has observed) before the arrival.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// try_wait with acquire at cluster scope: for barriers that CTAs of the
+// cluster other than this one arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// mbar_wait_bounded for barriers arrived on from other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t *bar, uint32_t parity,
+                                                          uint64_t limit_ns,
+                                                          volatile int *abort) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
+        }
+    }
 }
 
 // Cluster-wide barrier (all threads of all CTAs of the cluster); release /
@@ -169,6 +213,28 @@ __device__ __forceinline__ void tmem_relinquish() {
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+
+// The same three for a CTA pair (.cta_group::2: the two CTAs of a cluster
+// whose ranks differ in bit 0).  One warp of EACH CTA of the pair executes
+// the instruction; together they allocate (free) the same columns in both
+// CTAs' tensor memory, and each CTA's dst receives the address.  Every
+// tcgen05 instruction of a kernel that uses these takes .cta_group::2.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
                  "r"(ncols)
                  : "memory");
 }
@@ -218,22 +284,39 @@ __device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, u
         : "memory");
 }
 
+// The pair MMA (.cta_group::2), issued by one thread of one CTA of the pair:
+// D (256 x N) = A (256 x 16) * B (N x 16)^T.  Rows 0-127 of A are read from
+// the issuing CTA's shared memory and rows 128-255 from the peer's, both at
+// the descriptor's address; B's first N/2 rows (D's first N/2 columns) come
+// from the issuing CTA and the other N/2 from the peer; each CTA's tensor
+// memory at d_tmem receives its own 128 rows of D, all N columns.
+__device__ __forceinline__ void umma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on the mbarrier at the same offset in every CTA named in
+// cta_mask when every pair MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit_pair_multicast(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // Arrive (once) on the mbarrier when every tcgen05 operation this thread
 // issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
-        : "memory");
-}
-
-// As umma_commit, but the arrival goes to the mbarrier at the same offset in
-// every CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(cta_mask)
         : "memory");
 }
 

@@ -11,11 +11,12 @@
 // GB300 design (one persistent CTA per SM, 512 threads = 16 warps):
 //   warp 12     TMA producer: streams H [rows x 64] and W [<=256 x 64] k-blocks
 //               (128-byte swizzled) into a ring of 4-6 shared-memory stages; a whole
-//               W tile is one 256-row box (one 128-row box per CTA when
+//               W tile is one 256-row box (its 128-row half per CTA when
 //               paired), tails are 64- and 16-row boxes.
 //   warp 13     allocates 512 TMEM columns; one thread issues
-//               tcgen05.mma (M=128, N<=256, K=16, bf16 -> f32) into one of two
-//               256-column accumulators and commits to mbarriers.
+//               tcgen05.mma (M=128, N<=256, K=16, bf16 -> f32; paired CTAs:
+//               one M=256 MMA over both, issued by the even CTA) into one of
+//               two 256-column accumulators and commits to mbarriers.
 //   The producer and the MMA issuer share SM sub-partitions 0 and 1 with
 //   busy epilogue warps, so they issue as few instructions per k-block as
 //   possible (whole-tile boxes, precomputed descriptors).
@@ -61,6 +62,7 @@
 namespace fs {
 
 __device__ uint32_t g_status_word = 0;
+
 
 namespace {
 
@@ -273,12 +275,23 @@ __device__ __forceinline__ void store_bf16_chunk(__nv_bfloat16 *dst, int n,
 
 }  // namespace
 
-// CS = CTAs per cluster (1 or 2).  With CS = 2 the two CTAs of a cluster
-// work on consecutive batch tiles of the same vocabulary partition: each one
-// loads every other W box of a stage and multicasts it to both, so W crosses
-// L2 -> SM once per pair, and each stage is refilled only after both CTAs'
-// MMAs have released it (their commits arrive on both CTAs' empty barriers).
-template <int MODE, int CS>
+// PAIR selects the launch form.
+//   false  one CTA per (batch tile, partition).
+//   true   CTA pairs (2-CTA clusters) sharing one 256 x N MMA (.cta_group::2)
+//      over two consecutive batch tiles of the same vocabulary partition:
+//      each CTA loads its own 128 H rows and half of the tile's W rows, so a
+//      stage is 16 KB of H plus 16 KB of W per SM (6 stages fit instead of
+//      the 4 of a lone CTA's 48 KB stages), and W crosses L2 -> SM once per
+//      pair.  Both
+//      CTAs' loads of a stage complete on the leader's (the even CTA's) full
+//      barrier, whose expected byte count covers both halves, so the leader
+//      issues the MMAs of a stage once the whole pair's data has landed, with
+//      no per-stage message between the CTAs.  Its commits arrive on both
+//      CTAs' empty and full barriers.  Each CTA's epilogue reads its own 128
+//      accumulator lanes; the leader reuses an accumulator once both CTAs'
+//      epilogue warps have released it (the peer's warps arrive remotely on
+//      the leader's tempty_peer, once per tile).
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW16,
                   const __grid_constant__ CUtensorMap tmW64,
@@ -289,7 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                               MODE == kModeSampleXformLogprob);
     constexpr bool kLogprob = (MODE == kModeSampleLogprob || MODE == kModeSampleXformLogprob);
     constexpr bool kXform = (MODE == kModeSampleXform || MODE == kModeSampleXformLogprob);
+    constexpr int CS = PAIR ? 2 : 1;  // CTAs per cluster
+    constexpr bool kTwoSm = PAIR;
     constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CS) - 1u);
+    // bytes of one stage's W slot: half of a 256-row tile per CTA for the pair MMA
+    constexpr int kWSlot = kTwoSm ? kBBytes / 2 : kBBytes;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -308,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // slots or from the area in front of the ring, always inside shared
     // memory, and feed lanes that no epilogue warp reads.
     const int a_stride = (a.nM == 1) ? (a.h_box_rows * (kBK * 2) + 1023) & ~1023 : kABytes;
-    const int nst = min(kMaxStages, kRingBytes / (a_stride + kBBytes));
+    const int nst = min(kMaxStages, kRingBytes / (a_stride + kWSlot));
     const int lane_off = (a.nM != 1) ? 0 : (a.B <= 64 ? 64 : (a.B <= 96 ? 32 : 0));
     uint8_t *sA = smem + kPreRingBytes;
     uint8_t *sB = sA + nst * a_stride;
@@ -318,7 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *tfull_bar = bars + 2 * kMaxStages;
     uint64_t *tempty_bar = tfull_bar + 2;
     uint64_t *done_bar = tempty_bar + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done_bar + 1);
+    uint64_t *tempty_peer = done_bar + 1;  // leader, pair MMA: the peer's epilogue is done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty_peer + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *comb_s = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 256);
     int *comb_i = reinterpret_cast<int *>(comb_s + kColParts * kBM);
@@ -342,30 +360,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], CS);
+            mbar_init(&empty_bar[s], 1);  // one commit (the pair leader's when paired)
         }
         // Only epilogue warps whose TMEM lane quarter holds live batch rows
         // take part in the tile loop and release the accumulators.
-        int live_warps = 0;
-        for (int qq = 0; qq < 4; ++qq)
-            if (qq * 32 >= lane_off && (m * kBM + qq * 32 - lane_off) < a.B)
-                live_warps += quarter_parts(qq);
+        auto live_warps = [&](int mt) {
+            int n = 0;
+            for (int qq = 0; qq < 4; ++qq)
+                if (qq * 32 >= lane_off && (mt * kBM + qq * 32 - lane_off) < a.B)
+                    n += quarter_parts(qq);
+            return n;
+        };
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull_bar[i], 1);
-            mbar_init(&tempty_bar[i], live_warps);
+            mbar_init(&tempty_bar[i], live_warps(m));
+            // the peer's batch tile is m + 1 (it holds at least one row: the
+            // pair form runs only with an even number of batch tiles)
+            mbar_init(&tempty_peer[i], kTwoSm ? max(1, live_warps(m + 1)) : 1);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        if constexpr (kTwoSm) {
+            tmem_alloc_pair(tmem_slot, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    // Both CTAs' barriers must be initialised before either multicasts.
+    // Paired CTAs: both CTAs' barriers (and tensor memory) must be set up
+    // before either one's loads complete on, or its arrivals reach, the other.
     if (CS > 1) cluster_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -412,50 +442,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int v0, tn;
                 tile_geom(geom, t, v0, tn);
                 const int tn16 = round_up16(tn);
-                const int n64 = tn16 >> 6;
-                const int n16 = (tn16 & 63) >> 4;
-                const uint32_t bytes = h_bytes + tn16 * (kBK * 2);
+                // W rows this CTA loads per stage: the whole tile, or for the
+                // pair MMA its half of the tile rounded up to 32 rows (rows past
+                // the tile feed accumulator columns that no epilogue reads)
+                const int nw = kTwoSm ? ((tn + 31) & ~31) : tn16;
+                const int wrows = kTwoSm ? nw / 2 : tn16;
+                const int wrow0 = kTwoSm ? v0 + static_cast<int>(crank) * (nw / 2) : v0;
+                const int n64 = wrows >> 6;
+                const int n16 = (wrows & 63) >> 4;
+                const uint32_t bytes = h_bytes + wrows * (kBK * 2);
                 int kb = kb_first;
                 for (int j = 0; j < nk; ++j) {
                     if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, a.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full_bar[stage], bytes);
                     uint8_t *dA = sA + stage * a_stride;
-                    uint8_t *dB = sB + stage * kBBytes;
+                    uint8_t *dB = sB + stage * kWSlot;
                     const int kx = kb * kBK;
+                    if (kTwoSm) {
+                        // both CTAs' bytes of the stage complete on the leader's
+                        // full barrier; the leader expects them all (the peer's
+                        // loads may land before that, which only takes the byte
+                        // count below zero until the leader's arrival)
+                        const uint32_t bar =
+                            mapa_shared(smem_u32(&full_bar[stage]), 0u);
+                        if (crank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * bytes);
+                        tma_load_2d_pair(dA, &tmH, bar, kx, m * kBM, pol_h);
+                        if (wrows == kBN / 2) {
+                            tma_load_2d_pair(dB, &tmWhalf, bar, kx, wrow0, pol_w);
+                        } else {
+                            for (int i = 0; i < n64; ++i)
+                                tma_load_2d_pair(dB + i * 64 * (kBK * 2), &tmW64, bar, kx,
+                                                 wrow0 + i * 64, pol_w);
+                            for (int i = 0; i < n16; ++i)
+                                tma_load_2d_pair(dB + (n64 * 64 + i * 16) * (kBK * 2), &tmW16, bar,
+                                                 kx, wrow0 + n64 * 64 + i * 16, pol_w);
+                        }
+                        ++n_issued;
+                        if (++stage == nst) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        if (++kb == nk) kb = 0;
+                        continue;
+                    }
+                    mbar_arrive_expect_tx(&full_bar[stage], bytes);
                     tma_load_2d(dA, &tmH, &full_bar[stage], kx, m * kBM, pol_h);
                     if (tn16 == kBN) {
-                        // a whole tile: one box per CTA (half of it each, multicast, when
-                        // paired); same shared-memory layout as the 64-row boxes
-                        if (CS == 1)
-                            tma_load_2d(dB, &tmWfull, &full_bar[stage], kx, v0, pol_w);
-                        else
-                            tma_load_2d_multicast(dB + crank * (kBN / 2) * (kBK * 2), &tmWhalf,
-                                                  &full_bar[stage], kx,
-                                                  v0 + static_cast<int>(crank) * (kBN / 2),
-                                                  kClusterMask, pol_w);
-                    } else if (CS == 1) {
+                        // a whole tile: one box (same shared-memory layout as the
+                        // 64-row boxes)
+                        tma_load_2d(dB, &tmWfull, &full_bar[stage], kx, v0, pol_w);
+                    } else {
                         for (int i = 0; i < n64; ++i)
                             tma_load_2d(dB + i * 64 * (kBK * 2), &tmW64, &full_bar[stage], kx,
                                         v0 + i * 64, pol_w);
                         for (int i = 0; i < n16; ++i)
                             tma_load_2d(dB + (n64 * 64 + i * 16) * (kBK * 2), &tmW16,
                                         &full_bar[stage], kx, v0 + n64 * 64 + i * 16, pol_w);
-                    } else {
-                        // box i of the tile is loaded by cluster rank i % CS
-                        for (int i = static_cast<int>(crank); i < n64 + n16; i += CS) {
-                            if (i < n64)
-                                tma_load_2d_multicast(dB + i * 64 * (kBK * 2), &tmW64,
-                                                      &full_bar[stage], kx, v0 + i * 64,
-                                                      kClusterMask, pol_w);
-                            else
-                                tma_load_2d_multicast(
-                                    dB + (n64 * 64 + (i - n64) * 16) * (kBK * 2), &tmW16,
-                                    &full_bar[stage], kx, v0 + n64 * 64 + (i - n64) * 16,
-                                    kClusterMask, pol_w);
-                        }
                     }
                     ++n_issued;
                     if (++stage == nst) {
@@ -470,12 +514,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // memory is released (immediate on the normal path).
             // The last load into stage s is load number s + nst * ((n_issued - 1 - s) / nst);
             // its full barrier completes with parity (that number / nst) & 1.
-            for (int s = 0; s < nst && s < n_issued; ++s) {
+            // A pair-MMA peer's loads complete on the leader's barriers, which
+            // the leader drains (both CTAs stay resident until the cluster
+            // barrier at the end).
+            for (int s = 0; s < nst && s < n_issued && !(kTwoSm && crank != 0); ++s) {
                 const int last = s + nst * ((n_issued - 1 - s) / nst);
                 mbar_wait_bounded(&full_bar[s], static_cast<uint32_t>(last / nst) & 1u,
                                   a.timeout_ns, nullptr);
             }
         }
+    } else if (warp == kWarpMma && kTwoSm && crank != 0) {
+        // pair MMA, peer CTA: the leader issues every MMA; nothing to do here
     } else if (warp == kWarpMma) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -493,10 +542,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                // pair MMA: the peer's epilogue must have released it too
+                if (kTwoSm && !mbar_wait_bounded_cluster(&tempty_peer[acc], aphase ^ 1u,
+                                                         a.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after_sync();
                 int v0, tn;
                 tile_geom(geom, t, v0, tn);
-                const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(round_up16(tn)));
+                const uint32_t idesc =
+                    kTwoSm ? idesc_bf16_f32(2 * kBM, static_cast<uint32_t>((tn + 31) & ~31))
+                           : idesc_bf16_f32(kBM, static_cast<uint32_t>(round_up16(tn)));
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
                 for (int j = 0; j < nk; ++j) {
                     if (!mbar_wait_bounded(&full_bar[stage], phase, a.timeout_ns, abort_flag)) {
@@ -508,14 +565,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // descriptors differ from stage 0's by the stage offset and
                         // from each other by 32 bytes of K (both in 16-byte units)
                         const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage * (a_stride >> 4));
-                        const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (kBBytes >> 4));
+                        const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (kWSlot >> 4));
 #pragma unroll
-                        for (int ks = 0; ks < kBK / kUmmaK; ++ks)
-                            umma_bf16_ss(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc,
-                                         (j | ks) != 0 ? 1u : 0u);
+                        for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
+                            if constexpr (kTwoSm)
+                                umma_bf16_ss_pair(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc,
+                                                  (j | ks) != 0 ? 1u : 0u);
+                            else
+                                umma_bf16_ss(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc,
+                                             (j | ks) != 0 ? 1u : 0u);
+                        }
                     }
-                    if (CS > 1)
-                        umma_commit_multicast(&empty_bar[stage], kClusterMask);
+                    if constexpr (kTwoSm)
+                        umma_commit_pair_multicast(&empty_bar[stage], kClusterMask);
                     else
                         umma_commit(&empty_bar[stage]);
                     if (++stage == nst) {
@@ -523,11 +585,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         phase ^= 1u;
                     }
                 }
-                if (ok) umma_commit(&tfull_bar[acc]);
+                if (ok) {
+                    if constexpr (kTwoSm)
+                        umma_commit_pair_multicast(&tfull_bar[acc], kClusterMask);
+                    else
+                        umma_commit(&tfull_bar[acc]);
+                }
             }
             if (!ok) raise_timeout(abort_flag);
             // Retire every MMA this thread issued before TMEM is freed.
-            umma_commit(done_bar);
+            if constexpr (kTwoSm)
+                umma_commit_pair_multicast(done_bar, 1u);
+            else
+                umma_commit(done_bar);
             mbar_wait_bounded(done_bar, 0, a.timeout_ns, nullptr);
         }
     } else {
@@ -734,7 +804,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+            if (lane == 0) {
+                mbar_arrive(&tempty_bar[acc]);
+                // pair MMA: the leader reuses the accumulator only once the
+                // peer's warps have released it as well
+                if (kTwoSm && crank != 0)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_peer[acc]), 0u));
+            }
         }
         if (!ok) raise_timeout(abort_flag);
         if (kSample) {
@@ -782,29 +858,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // before reading.  Triggering only here keeps its blocks off the SMs while
     // the epilogues run.
     griddep_launch_dependents();
-    // No CTA leaves while its peer may still multicast into it or arrive on
-    // its barriers.
+    // Paired CTAs: neither leaves while the leader's MMAs may still read the
+    // peer's shared memory or write its tensor memory, or while the peer's
+    // arrivals may still reach the leader's barriers.
     if (CS > 1) cluster_sync();
     if (warp == kWarpMma) {
         __syncwarp();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (kTwoSm)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
-template <int MODE, int CS>
+template <int MODE, bool PAIR>
 static cudaError_t launch_mode(const CUtensorMap &tmH, const WMaps &wm, const Stage1Args &a,
                                int grid,
                                cudaStream_t stream) {
+    constexpr int CS = PAIR ? 2 : 1;
     static std::atomic<uint32_t> configured_mask{0};  // per device (device ordinals < 32)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 32 || !(configured_mask.load() & (1u << dev))) {
-        e = cudaFuncSetAttribute(stage1_kernel<MODE, CS>,
+        e = cudaFuncSetAttribute(stage1_kernel<MODE, PAIR>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         if (CS > 1) {
-            e = cudaFuncSetAttribute(stage1_kernel<MODE, CS>,
+            e = cudaFuncSetAttribute(stage1_kernel<MODE, PAIR>,
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
             if (e != cudaSuccess) return e;
         }
@@ -825,12 +906,12 @@ static cudaError_t launch_mode(const CUtensorMap &tmH, const WMaps &wm, const St
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, stage1_kernel<MODE, CS>, tmH, wm.w16, wm.w64, wm.w128,
+    return cudaLaunchKernelEx(&cfg, stage1_kernel<MODE, PAIR>, tmH, wm.w16, wm.w64, wm.w128,
                               wm.w256, a);
 }
 
-// How many 2-CTA clusters of Stage 1 the current device can hold at once
-// (cached per device; 0 if the query fails).
+// How many 2-CTA clusters of Stage 1's pair form the current device can hold
+// at once (cached per device; 0 if the query fails).
 static int max_pair_clusters() {
     static std::mutex mu;
     static int cached[64];
@@ -840,7 +921,7 @@ static int max_pair_clusters() {
     std::lock_guard<std::mutex> lock(mu);
     if (!known[dev]) {
         int n = 0;
-        if (cudaFuncSetAttribute(stage1_kernel<kModeSample, 2>,
+        if (cudaFuncSetAttribute(stage1_kernel<kModeSample, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -854,7 +935,7 @@ static int max_pair_clusters() {
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, stage1_kernel<kModeSample, 2>, &cfg) !=
+            if (cudaOccupancyMaxActiveClusters(&n, stage1_kernel<kModeSample, true>, &cfg) !=
                 cudaSuccess)
                 n = 0;
         }
@@ -865,42 +946,32 @@ static int max_pair_clusters() {
     return cached[dev];
 }
 
+template <bool PAIR>
+static cudaError_t launch_form(int mode, const CUtensorMap &tmH, const WMaps &wm,
+                               const Stage1Args &a, int grid, cudaStream_t stream) {
+    switch (mode) {
+        case kModeSample: return launch_mode<kModeSample, PAIR>(tmH, wm, a, grid, stream);
+        case kModeSampleStore:
+            return launch_mode<kModeSampleStore, PAIR>(tmH, wm, a, grid, stream);
+        case kModeGemmBf16: return launch_mode<kModeGemmBf16, PAIR>(tmH, wm, a, grid, stream);
+        case kModeGemmF32: return launch_mode<kModeGemmF32, PAIR>(tmH, wm, a, grid, stream);
+        case kModeSampleLogprob:
+            return launch_mode<kModeSampleLogprob, PAIR>(tmH, wm, a, grid, stream);
+        case kModeSampleXform:
+            return launch_mode<kModeSampleXform, PAIR>(tmH, wm, a, grid, stream);
+        case kModeSampleXformLogprob:
+            return launch_mode<kModeSampleXformLogprob, PAIR>(tmH, wm, a, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const WMaps &wm,
                           const Stage1Args &a, int grid,
                           cudaStream_t stream) {
     // Pairs only when batch tiles come in pairs and every pair fits at once.
     const bool pair = (a.nM % 2 == 0) && (2 * max_pair_clusters() >= grid);
-    if (pair) {
-        switch (mode) {
-            case kModeSample: return launch_mode<kModeSample, 2>(tmH, wm, a, grid, stream);
-            case kModeSampleStore:
-                return launch_mode<kModeSampleStore, 2>(tmH, wm, a, grid, stream);
-            case kModeGemmBf16:
-                return launch_mode<kModeGemmBf16, 2>(tmH, wm, a, grid, stream);
-            case kModeGemmF32: return launch_mode<kModeGemmF32, 2>(tmH, wm, a, grid, stream);
-            case kModeSampleLogprob:
-                return launch_mode<kModeSampleLogprob, 2>(tmH, wm, a, grid, stream);
-            case kModeSampleXform:
-                return launch_mode<kModeSampleXform, 2>(tmH, wm, a, grid, stream);
-            case kModeSampleXformLogprob:
-                return launch_mode<kModeSampleXformLogprob, 2>(tmH, wm, a, grid, stream);
-            default: return cudaErrorInvalidValue;
-        }
-    }
-    switch (mode) {
-        case kModeSample: return launch_mode<kModeSample, 1>(tmH, wm, a, grid, stream);
-        case kModeSampleStore:
-            return launch_mode<kModeSampleStore, 1>(tmH, wm, a, grid, stream);
-        case kModeGemmBf16: return launch_mode<kModeGemmBf16, 1>(tmH, wm, a, grid, stream);
-        case kModeGemmF32: return launch_mode<kModeGemmF32, 1>(tmH, wm, a, grid, stream);
-        case kModeSampleLogprob:
-            return launch_mode<kModeSampleLogprob, 1>(tmH, wm, a, grid, stream);
-        case kModeSampleXform:
-            return launch_mode<kModeSampleXform, 1>(tmH, wm, a, grid, stream);
-        case kModeSampleXformLogprob:
-            return launch_mode<kModeSampleXformLogprob, 1>(tmH, wm, a, grid, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    if (pair) return launch_form<true>(mode, tmH, wm, a, grid, stream);
+    return launch_form<false>(mode, tmH, wm, a, grid, stream);
 }
 
 cudaError_t status_word_address(uint32_t **out) {
