@@ -82,7 +82,18 @@ bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *p) {
         p->maxTiles = max_units <= kBN / kUnitRows
                           ? 1
                           : static_cast<int>((main_units + kBN / kUnitRows - 1) / (kBN / kUnitRows) + 1);
-    p->nChunks = static_cast<int>((V + kLogitsChunk - 1) / kLogitsChunk);
+    // materialised-logits sampler: about 4 blocks per SM over all B x V
+    // entries, each block a chunk of 2 K .. 64 K entries of one row
+    {
+        const int64_t want = (B * V) / (4 * static_cast<int64_t>(num_sms));
+        int64_t chunk = (want + kLogitsStep - 1) / kLogitsStep * kLogitsStep;
+        const int64_t vmax = (V + kLogitsStep - 1) / kLogitsStep * kLogitsStep;
+        if (chunk > kLogitsMaxChunk) chunk = kLogitsMaxChunk;
+        if (chunk > vmax) chunk = vmax;
+        if (chunk < kLogitsStep) chunk = kLogitsStep;
+        p->logitsChunk = static_cast<int>(chunk);
+        p->nChunks = static_cast<int>((V + chunk - 1) / chunk);
+    }
     const int64_t slots = p->nCand > p->nChunks ? p->nCand : p->nChunks;
     const int64_t region = ((slots * B * 4) + 255) / 256 * 256;
     p->wsBytes = static_cast<size_t>(kWorkspaceRegions * region);
@@ -966,7 +977,8 @@ fs_status fs_sample_from_logits(const void *Y, int y_dtype, int64_t B, int64_t V
     const Candidates cand = split_workspace(p, workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_logits_sample(Y, y_dtype, B, V, temperatures, temperature, seed,
-                                         offset, flags, cand.score, cand.idx, p.nChunks, s);
+                                         offset, flags, cand.score, cand.idx, p.nChunks,
+                                         p.logitsChunk, s);
     if (e != cudaSuccess) return cuda_fail(e, "logits sampling launch");
     e = launch_stage2(cand.score, cand.idx, p.nChunks, B, temperatures, temperature, out_idx,
                       out_score, s);

@@ -43,8 +43,13 @@ constexpr int kFinalTileUnits = 8;  // last tile of a partition: 128 rows
 constexpr int kUnitRows = 16;  // vocabulary partitions are multiples of 16 rows
 
 // ---- materialised-logits sampler ------------------------------------------
-constexpr int kLogitsChunk = 8192;  // vocabulary entries per block
+// A block scans one chunk of one row; the chunk (a multiple of one step,
+// 256 threads x 8 entries) grows with B * V up to 64 K entries, aiming at
+// about 4 blocks per SM, so that each thread scans a long run of its row and
+// the screen has a good running best to reject against.
 constexpr int kLogitsThreads = 256;
+constexpr int kLogitsStep = kLogitsThreads * 8;
+constexpr int kLogitsMaxChunk = 65536;
 
 enum Stage1Mode : int {
     kModeSample = 0,       // fused: GEMM + temperature + Gumbel + tile argmax
@@ -65,6 +70,7 @@ struct Plan {
     int64_t U;     // vocabulary units of 16 rows
     int maxTiles;  // max vocabulary tiles per CTA
     int nChunks;   // blocks per row of the materialised-logits sampler
+    int logitsChunk;  // vocabulary entries per block of that sampler
     size_t wsBytes;        // all five candidate arrays (log-probability and shard calls)
     size_t wsSampleBytes;  // the first two (score, index): what plain sampling uses
 };
@@ -137,7 +143,8 @@ cudaError_t launch_combine_groups(int64_t n_groups, int64_t B, const int64_t *gr
 cudaError_t launch_logits_sample(const void *Y, int y_dtype, int64_t B, int64_t V,
                                  const float *temps, float temp_scalar, uint64_t seed,
                                  uint64_t offset, uint32_t flags, float *cand_score,
-                                 int32_t *cand_idx, int nChunks, cudaStream_t stream);
+                                 int32_t *cand_idx, int nChunks, int chunk,
+                                 cudaStream_t stream);
 
 cudaError_t launch_upload(const void *src, void *dst, int64_t bytes, const float *tsrc,
                           float *tdst, int64_t nt, cudaStream_t stream);

@@ -307,14 +307,16 @@ cudaError_t launch_combine_groups(int64_t n_groups, int64_t B, const int64_t *gr
 }
 
 // ------------------------------------------------------------------ unfused sampling pass
-// Block (chunk, row): 256 threads scan kLogitsChunk logits of one row, 8 per
+// Block (chunk, row): 256 threads scan `chunk` logits of one row, 8 per
 // thread per step (one Philox call), then reduce to one candidate.  Like the
 // Stage 1 epilogue, each step screens its 8 elements against the thread's
 // best before the step (screen_lg2_tail / screen_bound) and pays for the
 // exact Gumbel only for the survivors, lowest index first; the screen is
-// conservative, so the result equals scoring every element.  The fused and
-// unfused paths then differ only by the logits' write and read-back, the
-// traffic the IO model counts.
+// conservative, so the result equals scoring every element.  A thread
+// scores its first element exactly and screens the rest of that step
+// against it, instead of scoring all 8.  The fused and unfused paths then
+// differ by the logits' write and read-back, the traffic the IO model
+// counts, and by the noise work that the fused kernel hides under its MMAs.
 template <typename T>
 __device__ __forceinline__ void load8(const T *row, int64_t v, int64_t v_end, bool vec_ok,
                                       float (&l)[8]);
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(kLogitsThreads)
     logits_sample_kernel(const T *__restrict__ Y, int64_t B, int64_t V,
                          const float *__restrict__ temps, float temp_scalar, uint64_t seed,
                          uint64_t offset, uint32_t flags, float *__restrict__ cand_score,
-                         int32_t *__restrict__ cand_idx, int nChunks, bool vec_ok) {
+                         int32_t *__restrict__ cand_idx, int chunk_len, bool vec_ok) {
     __shared__ float red_s[kLogitsThreads / 32];
     __shared__ uint32_t red_i[kLogitsThreads / 32];
     const int chunk = blockIdx.x;
@@ -365,14 +367,14 @@ __global__ void __launch_bounds__(kLogitsThreads)
         const float Tb = temps ? temps[b] : temp_scalar;
         const bool t_ok = temperature_ok(Tb);
         const float invT = __frcp_rn(Tb);
-        const int64_t v_begin = static_cast<int64_t>(chunk) * kLogitsChunk;
-        const int64_t v_end = min(V, v_begin + kLogitsChunk);
+        const int64_t v_begin = static_cast<int64_t>(chunk) * chunk_len;
+        const int64_t v_end = min(V, v_begin + chunk_len);
         const T *row = Y + b * V;
         const PhiloxRow prow = philox_row(seed, offset, static_cast<uint64_t>(b));
         float best = -INFINITY;
         uint32_t bi = 0xFFFFFFFFu;
         if (t_ok) {
-            for (int64_t v = v_begin + threadIdx.x * 8; v < v_end; v += kLogitsThreads * 8) {
+            for (int64_t v = v_begin + threadIdx.x * 8; v < v_end; v += kLogitsStep) {
                 float l[8];
                 load8<T>(row, v, v_end, vec_ok, l);
                 if (no_noise) {
@@ -391,11 +393,23 @@ __global__ void __launch_bounds__(kLogitsThreads)
                 float lt[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) lt[e] = __fmul_rn(l[e], invT);
+                // the thread's first element (v < v_end here) is scored
+                // exactly; the others are screened against the best so far
+                int first = 0;
+                if (best == -INFINITY) {
+                    const float s0 = __fadd_rn(lt[0], gumbel_from_word(x[0]));
+                    if (s0 > best) {
+                        best = s0;
+                        bi = static_cast<uint32_t>(v);
+                    }
+                    first = 1;
+                }
                 const float best0 = best;
                 uint32_t pass = 0;
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    if (v + e < v_end && screen_lg2_tail(x[e]) < screen_bound(lt[e], best0))
+                    if (e >= first && v + e < v_end &&
+                        screen_lg2_tail(x[e]) < screen_bound(lt[e], best0))
                         pass |= 1u << e;
                 while (pass) {
                     const int e = __ffs(pass) - 1;
@@ -438,19 +452,20 @@ __global__ void __launch_bounds__(kLogitsThreads)
 cudaError_t launch_logits_sample(const void *Y, int y_dtype, int64_t B, int64_t V,
                                  const float *temps, float temp_scalar, uint64_t seed,
                                  uint64_t offset, uint32_t flags, float *cand_score,
-                                 int32_t *cand_idx, int nChunks, cudaStream_t stream) {
+                                 int32_t *cand_idx, int nChunks, int chunk,
+                                 cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>(nChunks), static_cast<unsigned>(B < 65535 ? B : 65535));
     const uintptr_t base = reinterpret_cast<uintptr_t>(Y);
     if (y_dtype == 1) {
         const bool vec_ok = (base % 16 == 0) && (V % 4 == 0);
         logits_sample_kernel<float><<<grid, kLogitsThreads, 0, stream>>>(
             static_cast<const float *>(Y), B, V, temps, temp_scalar, seed, offset, flags,
-            cand_score, cand_idx, nChunks, vec_ok);
+            cand_score, cand_idx, chunk, vec_ok);
     } else {
         const bool vec_ok = (base % 16 == 0) && (V % 8 == 0);
         logits_sample_kernel<__nv_bfloat16><<<grid, kLogitsThreads, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(Y), B, V, temps, temp_scalar, seed, offset, flags,
-            cand_score, cand_idx, nChunks, vec_ok);
+            cand_score, cand_idx, chunk, vec_ok);
     }
     return cudaGetLastError();
 }

@@ -85,8 +85,17 @@ def test_plan_covers_the_vocabulary(B, V, D, sms):
         assert tiles <= p["max_tiles"]
         assert r1 > r0
     assert covered == V
-    slots = max(p["nCand"], (V + 8191) // 8192)
-    assert p["ws_bytes"] >= 8 * slots * B
+    slots = max(p["nCand"], logits_sampler_chunks(B, V, sms))
+    assert p["ws_bytes"] == 5 * ((slots * B * 4 + 255) // 256 * 256)
+
+
+def logits_sampler_chunks(B, V, sms):
+    """Blocks per row of the materialised-logits sampler: chunks of 2 K .. 64 K
+    entries (multiples of 2048), sized for about 4 blocks per SM over B x V."""
+    step = 2048
+    chunk = -(-(B * V // (4 * sms)) // step) * step
+    chunk = max(step, min(chunk, 65536, -(-V // step) * step))
+    return -(-V // chunk)
 
 
 def call_sample(H=16, W=16, B=4, V=64, D=64, T=1.0, temps=None, out=16):

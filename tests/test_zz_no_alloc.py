@@ -68,19 +68,27 @@ def test_noalloc_matches_fs_sample_on_two_calls(fs, B, V, D, T):
 
 def sample_scratch_bytes(B, V):
     """The two candidate arrays (score, index) plain sampling keeps: each
-    max(partitions, ceil(V / 8192)) x B four-byte values, rounded to 256 B."""
+    slots x B four-byte values, rounded to 256 B, where slots is the larger of
+    the vocabulary partitions and the blocks per row of the materialised-
+    logits sampler (chunks of 2 K .. 64 K entries, multiples of 2048, sized
+    for about 4 blocks per SM over B x V)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     parts = max(1, min(sms // ((B + 127) // 128), (V + 15) // 16))
-    slots = max(parts, (V + 8191) // 8192)
+    step = 2048
+    chunk = -(-(B * V // (4 * sms)) // step) * step
+    chunk = max(step, min(chunk, 65536, -(-V // step) * step))
+    slots = max(parts, -(-V // chunk))
     return 2 * ((slots * B * 4 + 255) // 256 * 256)
 
 
 def test_noalloc_takes_what_only_the_two_sampling_arrays_fit(fs):
-    """B = 4096 at V = 128256: the full workspace (five arrays, for the
-    log-probability calls) exceeds the scratch, the two arrays that sampling
-    keeps do not; the call is accepted and agrees with fs_sample."""
-    B, V, D = 4096, 128256, 64
-    assert fs.fs_workspace_size(B, V, D) > SCRATCH_BYTES >= sample_scratch_bytes(B, V)
+    """A shape whose full workspace (five arrays, for the log-probability
+    calls) exceeds the scratch while the two arrays that sampling keeps fit
+    (B = 8192 and about a million vocabulary entries on a 152-SM GPU): the
+    call is accepted and agrees with fs_sample."""
+    B, D = 8192, 64
+    V = next(v for v in range(600_000, 4_000_000, 65536)
+             if fs.fs_workspace_size(B, v, D) > SCRATCH_BYTES >= sample_scratch_bytes(B, v))
     g = torch.Generator(device="cpu").manual_seed(77)
     dev = torch.device("cuda:0")
     H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
@@ -93,7 +101,7 @@ def test_noalloc_takes_what_only_the_two_sampling_arrays_fit(fs):
 
 
 def test_noalloc_refuses_requests_beyond_its_scratch(fs):
-    B, V, D = 8192, 262144, 8
+    B, V, D = 262144, 16, 8
     assert sample_scratch_bytes(B, V) > SCRATCH_BYTES
     dev = torch.device("cuda:0")
     H = torch.zeros((B, D), dtype=torch.bfloat16, device=dev)
