@@ -225,6 +225,18 @@ __device__ __forceinline__ void apply_transforms(const Stage1Args &a, int b, int
     for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(l[i]);
 }
 
+// True when no element of a chunk can reach `best`: every l~ + g is below it
+// even with the largest Gumbel the noise can draw (kGumbelCeil).  NaN
+// elements are ignored (they never win); best = -inf keeps every chunk.
+__device__ __forceinline__ bool chunk_out_of_reach(const float (&lt)[16], int n_valid,
+                                                   float best) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if (i < n_valid) mx = fmaxf(mx, lt[i]);
+    return mx + kGumbelCeil < best;
+}
+
 __device__ __forceinline__ void epilogue_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(kNumEpiWarps * 32) : "memory");
 }
@@ -715,22 +727,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (kLogprob && i < n_valid && isfinite(s)) lse_add(lse_m, lse_s, s);
                                 }
                             } else {
-                                // Both Philox blocks of the chunk first (two
-                                // independent chains for the scheduler).
-                                if (!pre_noise) {
-                                    const uint64_t v8 =
-                                        static_cast<uint64_t>(a.vocab_offset + vbase) >> 3;
-                                    noise_words8(prow, v8, xa);
-                                    if (n_valid > 8) noise_words8(prow, v8 + 1, xb);
-                                }
                                 float lt[16];
 #pragma unroll
                                 for (int i = 0; i < 16; ++i)
                                     lt[i] = __fmul_rn(__uint_as_float(r[i]), invT);
-                                // A conservative screen per element against the
-                                // best known before the chunk (a lower bound of
-                                // the running best); survivors are scanned
-                                // exactly, in order.
                                 if (kLogprob) {
                                     // online log-sum-exp over the finite l~,
                                     // rescaled once per chunk
@@ -747,6 +747,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         if (i < n_valid && isfinite(lt[i]))
                                             lse_s += exp2_approx_scaled(lt[i] - lse_m);
                                 }
+                                // A chunk whose largest l~ lies more than the
+                                // largest Gumbel below the running best holds no
+                                // winner: its noise is never drawn.  The rows of a
+                                // warp share the chunk's columns, so with peaked
+                                // logits whole warps skip it.
+                                if (first_chunk || !chunk_out_of_reach(lt, n_valid, best)) {
+                                if (!pre_noise) {
+                                    const uint64_t v8 =
+                                        static_cast<uint64_t>(a.vocab_offset + vbase) >> 3;
+                                    noise_words8(prow, v8, xa);
+                                    if (n_valid > 8) noise_words8(prow, v8 + 1, xb);
+                                }
+                                // A conservative screen per element against the
+                                // best known before the chunk (a lower bound of
+                                // the running best); survivors are scanned
+                                // exactly, in order.
                                 const float best0 = best;
                                 if (first_chunk) {
                                     // every lane's best is still -inf: all 16
@@ -788,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     }
                                 }
                                 }  // not a first chunk
+                                }  // chunk within reach
                             }
                         }
                     } else if (row_ok) {

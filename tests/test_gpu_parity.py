@@ -129,6 +129,9 @@ def test_gumbel_transform_exhaustive(fs, dev):
     bad = err > 2 * ulp + 3e-7
     assert not bad.any(), "%d uniforms out of bound, first k = %d (err %g)" % (
         int(bad.sum()), int(k[bad][0]), float(err[bad][0]))
+    # Stage 1 skips a chunk whose logits are all more than 16.65 below the
+    # running best: no computed Gumbel may reach that ceiling
+    assert gg.max() < 16.65 - 1e-2, gg.max()
     # the series branch (u >= 15/16) holds the large Gumbels that win
     hi = k >= (15 << 20)
     print("gumbel: max |dg| = %.3e overall, %.3e for u >= 15/16; max in ulps %.2f" % (
@@ -165,6 +168,31 @@ def test_ragged_shapes(fs, dev, B, V, D):
     H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
     W = (torch.randn((V, D), generator=g) * (1.5 / D ** 0.5)).to(torch.bfloat16).to(dev)
     run_and_check(fs, H, W, 0.9, 1000 + B, 3, "B=%d V=%d D=%d" % (B, V, D))
+
+
+@pytest.mark.parametrize("B,V,D,T,spread", [(64, 50000, 64, 0.05, 1.0), (200, 60000, 128, 1.0, 12.0),
+                                             (256, 151936, 64, 0.8, 8.0), (3, 20011, 64, 0.01, 1.0)])
+def test_peaked_logits_where_most_chunks_are_out_of_reach(fs, dev, B, V, D, T, spread):
+    """Logits so spread out (large scale, or a small temperature) that most
+    16-column chunks lie more than the largest Gumbel below the running best
+    and draw no noise: every row still matches the oracle (the skip is exact),
+    and the unfused path, which scans each row differently, agrees bit for
+    bit.  A planted per-column bias (one column in 50 lifted) mimics the peaked
+    distribution of real LM heads."""
+    g = torch.Generator(device="cpu").manual_seed(B + V + int(100 * T))
+    H = torch.randn((B, D), generator=g)
+    H[:, D - 1] = 1.0
+    W = torch.randn((V, D), generator=g) * (spread / D ** 0.5)
+    lift = torch.rand(V, generator=g) < 0.02
+    W[:, D - 1] = torch.where(lift, torch.full((V,), 4.0 * spread), torch.full((V,), -4.0 * spread))
+    H = H.to(torch.bfloat16).to(dev)
+    W = W.to(torch.bfloat16).to(dev)
+    run_and_check(fs, H, W, T, 77 + B, 5, "peaked B=%d V=%d T=%g" % (B, V, T), store=False)
+    fi, fsc, _ = fs.fs_sample_ex(H, W, temperature=T, seed=77 + B, offset=5)
+    ui, usc, _ = fs.fs_sample_unfused(H, W, temperature=T, seed=77 + B, offset=5,
+                                      y_dtype=fs.FS_DTYPE_F32)
+    torch.cuda.synchronize()
+    assert torch.equal(fi, ui) and torch.equal(fsc, usc)
 
 
 def test_per_row_temperatures_with_invalid_rows(fs, dev):

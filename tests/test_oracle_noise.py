@@ -154,3 +154,17 @@ def test_offsets_and_rows_give_independent_streams():
     d, _ = oracle.noise_block(6, 0, 0, 1, 0, 4096)
     for other in (b, c, d):
         assert np.count_nonzero(a == other) <= 2
+
+
+def test_largest_gumbel_sits_below_the_skip_ceiling():
+    """The largest uniform is u = 1 - 2^-24, so no Gumbel exceeds
+    -log(-log(1 - 2^-24)) = 16.6355...; the GPU skips any 16-column chunk whose
+    logits all lie more than 16.65 below the running best, which is exact only
+    because every Gumbel (oracle: all 2^23 distinct uniforms) stays clearly
+    below that ceiling."""
+    k = np.arange(1, 1 << 24, 2, dtype=np.uint32)
+    g = oracle.gumbel_block(k << np.uint32(8))
+    g_max = -math.log(-math.log1p(-2.0 ** -24))
+    assert abs(float(g.max()) - g_max) < 1e-5
+    assert float(g.max()) < 16.65 - 1e-2
+    assert int(np.argmax(g)) == len(k) - 1  # at u = 1 - 2^-24
