@@ -26,10 +26,10 @@
  *     returns FS_ERR_UNSUPPORTED and launches nothing.
  *   - H and W must be device memory of the current GPU (cudaMalloc-family or
  *     pool memory of that device).  Stage 1 reads them with tensor-memory
- *     loads, and its paired form (two CTAs of a cluster sharing each W tile)
- *     multicasts every W box into both CTAs; those loads are kept to the
- *     calling GPU's own memory.  Page-locked host memory, another GPU's
- *     memory (peer access) and managed memory are refused with
+ *     loads, and in its paired form (two CTAs of a cluster sharing one MMA)
+ *     both CTAs' loads complete on one CTA's barrier; those loads are kept
+ *     to the calling GPU's own memory.  Page-locked host memory, another
+ *     GPU's memory (peer access) and managed memory are refused with
  *     FS_ERR_UNSUPPORTED before anything is launched.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are asynchronous on `stream`: a returned FS_OK means the

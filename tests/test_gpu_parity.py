@@ -550,9 +550,9 @@ def test_sample_from_materialised_logits(fs, dev, dtype, B, V):
 
 # ---------------------------------------------------------------- full-size workloads
 
-# (workload, B): one batch tile (stage1_kernel<sample, 1>) for B <= 128 and
-# an odd number of batch tiles; paired CTAs (stage1_kernel<sample, 2>, W
-# multicast inside a cluster) for an even number of batch tiles.
+# (workload, B): one batch tile (stage1_kernel<sample, false>) for B <= 128
+# and an odd number of batch tiles; CTA pairs sharing one M=256 MMA
+# (stage1_kernel<sample, true>) for an even number of batch tiles.
 FULL = [("llama3_8b", 64), ("llama3_8b", 1), ("qwen", 256), ("qwen", 100),
         ("llama3_70b", 256), ("llama3_70b", 512), ("llama3_70b", 1024), ("bigvocab", 512),
         ("bigvocab", 64), ("bigvocab", 1)]
