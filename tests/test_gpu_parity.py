@@ -195,9 +195,12 @@ def test_peaked_logits_where_most_chunks_are_out_of_reach(fs, dev, B, V, D, T, s
     assert torch.equal(fi, ui) and torch.equal(fsc, usc)
 
 
-def test_per_row_temperatures_with_invalid_rows(fs, dev):
-    B, V, D = 40, 3000, 128
-    g = torch.Generator(device="cpu").manual_seed(4)
+@pytest.mark.parametrize("B", [40, 256])
+def test_per_row_temperatures_with_invalid_rows(fs, dev, B):
+    """Invalid per-row temperatures give -1 / NaN for their rows only, in a
+    single batch tile (B=40) and in the paired kernel (B=256)."""
+    V, D = 3000, 128
+    g = torch.Generator(device="cpu").manual_seed(4 + B)
     H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
     W = (torch.randn((V, D), generator=g) * 0.1).to(torch.bfloat16).to(dev)
     T = 0.5 + torch.rand(B, generator=g)
@@ -207,7 +210,10 @@ def test_per_row_temperatures_with_invalid_rows(fs, dev):
     T[19] = float("nan")
     T[23] = 1e-3
     T[29] = 1e3
-    run_and_check(fs, H, W, T.to(dev), 77, 1, "per-row T")
+    if B > 128:
+        T[130] = 0.0     # in the peer CTA's batch tile
+        T[255] = float("nan")
+    run_and_check(fs, H, W, T.to(dev), 77, 1, "per-row T B=%d" % B)
 
 
 def test_no_noise_ties_go_to_lowest_index(fs, dev):
@@ -669,7 +675,8 @@ def _mask(rng, B, V, keep=0.7):
 
 @pytest.mark.parametrize("B,V,D,softcap,use_bias,use_mask", [
     (37, 9001, 128, 0.0, True, False), (64, 40000, 64, 30.0, True, True),
-    (5, 4099, 136, 10.0, False, True), (260, 20011, 64, 0.0, True, True)])
+    (5, 4099, 136, 10.0, False, True), (260, 20011, 64, 0.0, True, True),
+    (256, 30011, 96, 25.0, True, True)])
 def test_transforms_match_oracle(fs, dev, B, V, D, softcap, use_bias, use_mask):
     rng = np.random.default_rng(B + V)
     g = torch.Generator(device="cpu").manual_seed(B * 5 + V)
