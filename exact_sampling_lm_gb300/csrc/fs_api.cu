@@ -94,24 +94,26 @@ bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *p) {
         p->logitsChunk = static_cast<int>(chunk);
         p->nChunks = static_cast<int>((V + chunk - 1) / chunk);
     }
+    auto region = [&](int64_t slots) { return ((slots * B * 4) + 255) / 256 * 256; };
     const int64_t slots = p->nCand > p->nChunks ? p->nCand : p->nChunks;
-    const int64_t region = ((slots * B * 4) + 255) / 256 * 256;
-    p->wsBytes = static_cast<size_t>(kWorkspaceRegions * region);
-    p->wsSampleBytes = static_cast<size_t>(2 * region);
+    p->wsBytes = static_cast<size_t>(kWorkspaceRegions * region(slots));
+    p->wsSampleBytes = static_cast<size_t>(2 * region(p->nCand));
+    p->wsLogprobBytes = static_cast<size_t>(kWorkspaceRegions * region(p->nCand));
+    p->wsLogitsBytes = static_cast<size_t>(2 * region(p->nChunks));
     return true;
 }
 
 // Candidate buffers inside a workspace, each [slots][B] of 4-byte values:
 // score, index, and (log-probability calls only) the winner's l~ and the
-// log-mass pair (max, sum).
+// log-mass pair (max, sum).  slots: p.nCand for the fused calls, p.nChunks
+// for the materialised-logits sampler.
 struct Candidates {
     float *score;
     int32_t *idx;
     float *lt, *m, *s;
 };
 
-static Candidates split_workspace(const Plan &p, void *ws) {
-    const int64_t slots = p.nCand > p.nChunks ? p.nCand : p.nChunks;
+static Candidates split_workspace(const Plan &p, void *ws, int64_t slots) {
     const int64_t region = ((slots * p.B * 4) + 255) / 256 * 256;
     char *base = static_cast<char *>(ws);
     Candidates c;
@@ -539,7 +541,7 @@ fs_status fs_stage1(const void *H, const void *W, int64_t B, int64_t V, int64_t 
     Plan p;
     make_plan(B, V, D, info.sms, &p);
     if ((st = validate_workspace(workspace, ws_bytes, p.wsSampleBytes)) != FS_OK) return st;
-    const Candidates cand = split_workspace(p, workspace);
+    const Candidates cand = split_workspace(p, workspace, p.nCand);
     const int mode = (flags & FS_FLAG_STORE_LOGITS) ? kModeSampleStore : kModeSample;
     return run_stage1(mode, H, W, p, temperature, temperatures, seed, offset, flags,
                       (flags & FS_FLAG_STORE_LOGITS) ? out_logits : nullptr, nullptr, 0, &cand,
@@ -560,7 +562,7 @@ fs_status fs_stage2(int64_t B, int64_t V, int64_t D, float temperature,
     Plan p;
     make_plan(B, V, D, info.sms, &p);
     if ((st = validate_workspace(workspace, ws_bytes, p.wsSampleBytes)) != FS_OK) return st;
-    const Candidates cand = split_workspace(p, const_cast<void *>(workspace));
+    const Candidates cand = split_workspace(p, const_cast<void *>(workspace), p.nCand);
     cudaError_t e = launch_stage2(cand.score, cand.idx, p.nCand, B, temperatures, temperature,
                                   out_idx, out_score, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "Stage 2 launch");
@@ -810,8 +812,8 @@ fs_status fs_sample_logprob(const void *H, const void *W, int64_t B, int64_t V, 
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
     Plan p;
     make_plan(B, V, D, info.sms, &p);
-    if ((st = validate_workspace(workspace, ws_bytes, p.wsBytes)) != FS_OK) return st;
-    const Candidates cand = split_workspace(p, workspace);
+    if ((st = validate_workspace(workspace, ws_bytes, p.wsLogprobBytes)) != FS_OK) return st;
+    const Candidates cand = split_workspace(p, workspace, p.nCand);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = run_stage1(kModeSampleLogprob, H, W, p, temperature, temperatures, seed, offset, 0,
                          nullptr, nullptr, 0, &cand, s)) != FS_OK)
@@ -856,10 +858,10 @@ fs_status fs_sample_transformed(const void *H, const void *W, int64_t B, int64_t
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
     Plan p;
     make_plan(B, V, D, info.sms, &p);
-    if ((st = validate_workspace(workspace, ws_bytes, out_logprob ? p.wsBytes : p.wsSampleBytes)) !=
+    if ((st = validate_workspace(workspace, ws_bytes, out_logprob ? p.wsLogprobBytes : p.wsSampleBytes)) !=
         FS_OK)
         return st;
-    const Candidates cand = split_workspace(p, workspace);
+    const Candidates cand = split_workspace(p, workspace, p.nCand);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int mode = out_logprob ? kModeSampleXformLogprob : kModeSampleXform;
     if ((st = run_stage1(mode, H, W, p, temperature, temperatures, seed, offset, flags, nullptr,
@@ -898,8 +900,8 @@ fs_status fs_sample_shard(const void *H, const void *W_shard, int64_t B, int64_t
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
     Plan p;
     make_plan(B, V_shard, D, info.sms, &p);
-    if ((st = validate_workspace(workspace, ws_bytes, p.wsBytes)) != FS_OK) return st;
-    const Candidates cand = split_workspace(p, workspace);
+    if ((st = validate_workspace(workspace, ws_bytes, p.wsLogprobBytes)) != FS_OK) return st;
+    const Candidates cand = split_workspace(p, workspace, p.nCand);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = run_stage1(kModeSampleLogprob, H, W_shard, p, temperature, temperatures, seed,
                          offset, 0, nullptr, nullptr, 0, &cand, s, nullptr, vocab_offset)) !=
@@ -974,8 +976,8 @@ fs_status fs_sample_from_logits(const void *Y, int y_dtype, int64_t B, int64_t V
     if ((st = device_info(&dev, &info)) != FS_OK) return st;
     Plan p;
     make_plan(B, V, 8, info.sms, &p);
-    if ((st = validate_workspace(workspace, ws_bytes, p.wsSampleBytes)) != FS_OK) return st;
-    const Candidates cand = split_workspace(p, workspace);
+    if ((st = validate_workspace(workspace, ws_bytes, p.wsLogitsBytes)) != FS_OK) return st;
+    const Candidates cand = split_workspace(p, workspace, p.nChunks);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_logits_sample(Y, y_dtype, B, V, temperatures, temperature, seed,
                                          offset, flags, cand.score, cand.idx, p.nChunks,

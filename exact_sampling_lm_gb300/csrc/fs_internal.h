@@ -71,8 +71,13 @@ struct Plan {
     int maxTiles;  // max vocabulary tiles per CTA
     int nChunks;   // blocks per row of the materialised-logits sampler
     int logitsChunk;  // vocabulary entries per block of that sampler
-    size_t wsBytes;        // all five candidate arrays (log-probability and shard calls)
-    size_t wsSampleBytes;  // the first two (score, index): what plain sampling uses
+    // Workspace bytes.  Every call lays out its candidate arrays, each
+    // [slots][B] of 4-byte values rounded up to 256 B, with the slots it uses:
+    // nCand for the fused calls, nChunks for the materialised-logits sampler.
+    size_t wsBytes;        // fs_workspace_size: five arrays of max(nCand, nChunks) slots
+    size_t wsSampleBytes;  // fused sampling: two arrays (score, index) of nCand slots
+    size_t wsLogprobBytes; // fused sampling with log-masses: five arrays of nCand slots
+    size_t wsLogitsBytes;  // materialised-logits sampler: two arrays of nChunks slots
 };
 
 bool make_plan(int64_t B, int64_t V, int64_t D, int num_sms, Plan *plan);

@@ -71,7 +71,7 @@ extern "C" fs_status fs_sample_noalloc(const void *H, const void *W, int64_t B, 
                                        uint64_t seed, uint64_t offset, int64_t *out_idx,
                                        float *out_score, void *stream) {
     // Plain sampling keeps two candidate arrays (score, index), each of
-    // max(partitions, ceil(V / 8192)) x B four-byte values rounded up to 256 B.
+    // partitions x B four-byte values rounded up to 256 B.
     const size_t need = fs::sample_workspace_bytes(B, V, D);
     if (need == 0) {
         // bad arguments or no usable device: let the regular entry point

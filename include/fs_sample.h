@@ -358,11 +358,11 @@ fs_status fs_plan_info(int64_t B, int64_t V, int64_t D, int num_sms, int64_t out
  * Arguments, results and errors are those of fs_sample.  The candidate
  * scratch is a static array of FS_NOALLOC_SCRATCH_BYTES inside the library's
  * device memory (held on every GPU that loads the library until the process
- * exits).  A call keeps two candidate arrays (score, index) of
- * max(partitions, ceil(V / 8192)) x B four-byte values each, rounded up to
- * 256 bytes (partitions = floor(SMs / ceil(B / 128)), at least 1); a call
- * that needs more than the array returns FS_ERR_UNSUPPORTED and launches
- * nothing (on a 152-SM GPU every B up to 8192 fits at V = 128256).
+ * exits).  A call keeps two candidate arrays (score, index) of P x B
+ * four-byte values each, rounded up to 256 bytes, where P = the vocabulary
+ * partitions of Stage 1 = min(floor(SMs / ceil(B / 128)), ceil(V / 16)), at
+ * least 1; a call that needs more than the array returns FS_ERR_UNSUPPORTED
+ * and launches nothing (on a 152-SM GPU every B up to 131072 fits).
  * The first call in each CUDA context looks up the array's device address
  * (cudaGetSymbolAddress), so make that first call before any stream capture.
  * All calls share the array: calls whose kernels overlap on the GPU (other

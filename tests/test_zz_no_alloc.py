@@ -68,26 +68,19 @@ def test_noalloc_matches_fs_sample_on_two_calls(fs, B, V, D, T):
 
 def sample_scratch_bytes(B, V):
     """The two candidate arrays (score, index) plain sampling keeps: each
-    slots x B four-byte values, rounded to 256 B, where slots is the larger of
-    the vocabulary partitions and the blocks per row of the materialised-
-    logits sampler (chunks of 2 K .. 64 K entries, multiples of 2048, sized
-    for about 4 blocks per SM over B x V)."""
+    P x B four-byte values rounded to 256 B, P being Stage 1's vocabulary
+    partitions, min(SMs // ceil(B / 128), ceil(V / 16)), at least 1."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     parts = max(1, min(sms // ((B + 127) // 128), (V + 15) // 16))
-    step = 2048
-    chunk = -(-(B * V // (4 * sms)) // step) * step
-    chunk = max(step, min(chunk, 65536, -(-V // step) * step))
-    slots = max(parts, -(-V // chunk))
-    return 2 * ((slots * B * 4 + 255) // 256 * 256)
+    return 2 * ((parts * B * 4 + 255) // 256 * 256)
 
 
 def test_noalloc_takes_what_only_the_two_sampling_arrays_fit(fs):
-    """A shape whose full workspace (five arrays, for the log-probability
-    calls) exceeds the scratch while the two arrays that sampling keeps fit
-    (B = 8192 and about a million vocabulary entries on a 152-SM GPU): the
-    call is accepted and agrees with fs_sample."""
-    B, D = 8192, 64
-    V = next(v for v in range(600_000, 4_000_000, 65536)
+    """A shape whose full workspace (five arrays wide enough for every entry
+    point) exceeds the scratch while the two arrays that sampling keeps fit:
+    the call is accepted and agrees with fs_sample."""
+    B, D = 32768, 64
+    V = next(v for v in (4096, 16384, 65536, 262144)
              if fs.fs_workspace_size(B, v, D) > SCRATCH_BYTES >= sample_scratch_bytes(B, v))
     g = torch.Generator(device="cpu").manual_seed(77)
     dev = torch.device("cuda:0")
