@@ -154,7 +154,7 @@ def test_tiny_workload(fs, dev):
     (127, 2000, 64), (128, 2048, 128), (129, 3001, 64), (255, 1000, 520),
     (300, 5003, 200), (2, 50257, 64), (33, 40000, 64), (130, 41000, 96),
     (16, 45000, 136), (17, 45000, 136), (88, 45000, 200), (89, 45000, 200),
-    (96, 45000, 64), (97, 45000, 64),
+    (96, 45000, 64), (97, 45000, 64), (256, 1000, 8192), (256, 64, 65536),
 ])
 def test_ragged_shapes(fs, dev, B, V, D):
     """Batch tails (B not a multiple of 128), vocabulary tails (V not a
@@ -163,7 +163,8 @@ def test_ragged_shapes(fs, dev, B, V, D):
     88 / 89 sit on the ring-depth boundaries of a single batch tile (6, 5 and
     4 stages), with several tiles per CTA so the last tile's parked noise is
     used too; B = 33, 64 / 65 and 96 / 97 on the accumulator-lane offsets
-    (64, 32, 0) of a single batch tile."""
+    (64, 32, 0) of a single batch tile; B = 256 with D = 8192 and 65536 runs
+    the paired kernel over 128 and 1024 k-blocks per tile."""
     g = torch.Generator(device="cpu").manual_seed(B * 7919 + V * 31 + D)
     H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
     W = (torch.randn((V, D), generator=g) * (1.5 / D ** 0.5)).to(torch.bfloat16).to(dev)
