@@ -875,6 +875,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // before reading.  Triggering only here keeps its blocks off the SMs while
     // the epilogues run.
     griddep_launch_dependents();
+    // Pair MMA after a timeout anywhere (the device error word is set): the
+    // peer's loads complete only on the leader's barriers, and the leader
+    // drains no further than the phases it armed, so the peer gives any load
+    // still in flight a bounded 100 us to land before the pair releases its
+    // shared memory.  On the normal path every load was consumed by an MMA.
+    if (kTwoSm && crank != 0 && threadIdx.x == 0 &&
+        *reinterpret_cast<volatile uint32_t *>(&g_status_word) != 0u) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 100000ull) {
+        }
+    }
     // Paired CTAs: neither leaves while the leader's MMAs may still read the
     // peer's shared memory or write its tensor memory, or while the peer's
     // arrivals may still reach the leader's barriers.
