@@ -327,8 +327,9 @@ static const char *memory_type_name(cudaMemoryType t) {
 }
 
 // The TMA tensor maps of Stage 1 are encoded on the caller's H and W, and in
-// the paired kernel the two CTAs of a cluster feed one MMA from both CTAs'
-// shared memory, their loads completing on one CTA's barrier.  Those loads
+// the paired forms the two CTAs of a cluster either multicast W boxes to
+// each other or feed one MMA from both CTAs' shared memory, their loads
+// completing on one CTA's barrier.  Those loads
 // must read this GPU's own memory: not host memory reached through a
 // mapping, not another GPU's memory reached through peer access, not managed
 // memory that may migrate.  Anything else is refused before a launch.

@@ -151,13 +151,6 @@ __device__ __forceinline__ float gumbel_from_word(uint32_t x) {
     return -0.69314718055994531f * lg2_approx(w);
 }
 
-// An upper bound of every Gumbel gumbel_from_word can return.  The largest
-// uniform is u = 1 - 2^-24, whose Gumbel is -log(-log u) = 16.63553; the
-// bound adds 0.0145, far above the computed Gumbel's error (a few 1e-6) and
-// the rounding of a score of that size (below 1e-6).  An element whose
-// l~ + kGumbelCeil is below the best score found so far can never win.
-constexpr float kGumbelCeil = 16.65f;
-
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

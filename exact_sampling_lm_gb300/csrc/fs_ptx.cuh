@@ -130,6 +130,22 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorM
         : "memory");
 }
 
+// Multicast form: one box is written to the same shared-memory offset in
+// every CTA of the cluster named in cta_mask, and its bytes complete on the
+// mbarrier at the same offset in each of those CTAs.  The source must be
+// memory of this GPU.
+__device__ __forceinline__ void tma_load_2d_multicast(void *smem_dst, const CUtensorMap *map,
+                                                      uint64_t *bar, int32_t x, int32_t y,
+                                                      uint16_t cta_mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask),
+        "l"(policy)
+        : "memory");
+}
+
 // Prefetch one tensor-map box into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -298,6 +314,16 @@ __device__ __forceinline__ void umma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_de
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on the mbarrier at the same offset in every CTA named in
+// cta_mask when every single-CTA MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
         : "memory");
 }
 

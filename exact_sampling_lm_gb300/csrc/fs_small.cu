@@ -314,8 +314,7 @@ cudaError_t launch_combine_groups(int64_t n_groups, int64_t B, const int64_t *gr
 // exact Gumbel only for the survivors, lowest index first; the screen is
 // conservative, so the result equals scoring every element.  A thread
 // scores its first element exactly and screens the rest of that step
-// against it, instead of scoring all 8; a step whose logits all lie more
-// than the largest Gumbel below the thread's best draws no noise at all.  The fused and unfused paths then
+// against it, instead of scoring all 8.  The fused and unfused paths then
 // differ by the logits' write and read-back, the traffic the IO model
 // counts, and by the noise work that the fused kernel hides under its MMAs.
 template <typename T>
@@ -389,21 +388,11 @@ __global__ void __launch_bounds__(kLogitsThreads)
                     }
                     continue;
                 }
+                uint32_t x[8];
+                noise_words8(prow, static_cast<uint64_t>(v) >> 3, x);
                 float lt[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) lt[e] = __fmul_rn(l[e], invT);
-                // as in Stage 1: no element of the step can reach the best
-                // found so far, even with the largest Gumbel, so its noise is
-                // never drawn (NaN entries are ignored: they never win)
-                {
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        if (v + e < v_end) mx = fmaxf(mx, lt[e]);
-                    if (mx + kGumbelCeil < best) continue;
-                }
-                uint32_t x[8];
-                noise_words8(prow, static_cast<uint64_t>(v) >> 3, x);
                 // the thread's first element (v < v_end here) is scored
                 // exactly; the others are screened against the best so far
                 int first = 0;

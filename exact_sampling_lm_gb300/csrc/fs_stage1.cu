@@ -12,11 +12,13 @@
 //   warp 12     TMA producer: streams H [rows x 64] and W [<=256 x 64] k-blocks
 //               (128-byte swizzled) into a ring of 4-6 shared-memory stages; a whole
 //               W tile is one 256-row box (its 128-row half per CTA when
-//               paired), tails are 64- and 16-row boxes.
+//               paired: multicast to both CTAs, or kept for a shared MMA),
+//               tails are 64- and 16-row boxes.
 //   warp 13     allocates 512 TMEM columns; one thread issues
-//               tcgen05.mma (M=128, N<=256, K=16, bf16 -> f32; paired CTAs:
-//               one M=256 MMA over both, issued by the even CTA) into one of
-//               two 256-column accumulators and commits to mbarriers.
+//               tcgen05.mma (M=128, N<=256, K=16, bf16 -> f32; at large D
+//               paired CTAs run one M=256 MMA over both, issued by the even
+//               CTA) into one of two 256-column accumulators and commits to
+//               mbarriers.
 //   The producer and the MMA issuer share SM sub-partitions 0 and 1 with
 //   busy epilogue warps, so they issue as few instructions per k-block as
 //   possible (whole-tile boxes, precomputed descriptors).
@@ -67,6 +69,15 @@ __device__ uint32_t g_status_word = 0;
 namespace {
 
 constexpr uint32_t kStatusTimeout = 1u;
+
+// Stage 1 launch forms (see stage1_kernel)
+constexpr int kFormSingle = 0;
+constexpr int kFormMulticast = 1;
+constexpr int kFormPairMma = 2;
+// the pair MMA serves paired calls with D at least this: with two batch
+// tiles, or with more
+constexpr int kPairMmaMinD2 = 4096;
+constexpr int kPairMmaMinD = 6144;
 
 __device__ __forceinline__ int round_up16(int x) { return (x + 15) & ~15; }
 
@@ -225,18 +236,6 @@ __device__ __forceinline__ void apply_transforms(const Stage1Args &a, int b, int
     for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(l[i]);
 }
 
-// True when no element of a chunk can reach `best`: every l~ + g is below it
-// even with the largest Gumbel the noise can draw (kGumbelCeil).  NaN
-// elements are ignored (they never win); best = -inf keeps every chunk.
-__device__ __forceinline__ bool chunk_out_of_reach(const float (&lt)[16], int n_valid,
-                                                   float best) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        if (i < n_valid) mx = fmaxf(mx, lt[i]);
-    return mx + kGumbelCeil < best;
-}
-
 __device__ __forceinline__ void epilogue_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(kNumEpiWarps * 32) : "memory");
 }
@@ -287,23 +286,29 @@ __device__ __forceinline__ void store_bf16_chunk(__nv_bfloat16 *dst, int n,
 
 }  // namespace
 
-// PAIR selects the launch form.
-//   false  one CTA per (batch tile, partition).
-//   true   CTA pairs (2-CTA clusters) sharing one 256 x N MMA (.cta_group::2)
-//      over two consecutive batch tiles of the same vocabulary partition:
-//      each CTA loads its own 128 H rows and half of the tile's W rows, so a
-//      stage is 16 KB of H plus 16 KB of W per SM (6 stages fit instead of
-//      the 4 of a lone CTA's 48 KB stages), and W crosses L2 -> SM once per
-//      pair.  Both
-//      CTAs' loads of a stage complete on the leader's (the even CTA's) full
-//      barrier, whose expected byte count covers both halves, so the leader
-//      issues the MMAs of a stage once the whole pair's data has landed, with
-//      no per-stage message between the CTAs.  Its commits arrive on both
-//      CTAs' empty and full barriers.  Each CTA's epilogue reads its own 128
-//      accumulator lanes; the leader reuses an accumulator once both CTAs'
-//      epilogue warps have released it (the peer's warps arrive remotely on
-//      the leader's tempty_peer, once per tile).
-template <int MODE, bool PAIR>
+// FORM selects the launch form.
+//   kFormSingle     one CTA per (batch tile, partition).
+//   kFormMulticast  CTA pairs (2-CTA clusters) over two consecutive batch
+//      tiles of the same vocabulary partition, each with its own M=128 MMA:
+//      each CTA loads half of every W k-block and multicasts it to both, so
+//      W crosses L2 -> SM once per pair.  A stage is refilled only after both
+//      CTAs' MMAs have released it (each CTA's commit arrives on both CTAs'
+//      empty barriers).
+//   kFormPairMma    CTA pairs sharing one 256 x N MMA (.cta_group::2): each
+//      CTA loads its own 128 H rows and half of the tile's W rows, so a stage
+//      is 16 KB of H plus 16 KB of W per SM (6 stages fit instead of the 4 of
+//      48 KB stages).  Both CTAs' loads of a stage complete on the leader's
+//      (the even CTA's) full barrier, whose expected byte count covers both
+//      halves, so the leader issues the MMAs of a stage once the whole pair's
+//      data has landed, with no per-stage message between the CTAs.  Its
+//      commits arrive on both CTAs' empty and full barriers.  Each CTA's
+//      epilogue reads its own 128 accumulator lanes; the leader reuses an
+//      accumulator once both CTAs' epilogue warps have released it (the
+//      peer's warps arrive remotely on the leader's tempty_peer, once per
+//      tile).
+//   Both pair forms move the same bytes; which is faster depends on D (see
+//   launch_stage1).
+template <int MODE, int FORM>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW16,
                   const __grid_constant__ CUtensorMap tmW64,
@@ -314,8 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                               MODE == kModeSampleXformLogprob);
     constexpr bool kLogprob = (MODE == kModeSampleLogprob || MODE == kModeSampleXformLogprob);
     constexpr bool kXform = (MODE == kModeSampleXform || MODE == kModeSampleXformLogprob);
-    constexpr int CS = PAIR ? 2 : 1;  // CTAs per cluster
-    constexpr bool kTwoSm = PAIR;
+    constexpr int CS = FORM == kFormSingle ? 1 : 2;  // CTAs per cluster
+    constexpr bool kTwoSm = FORM == kFormPairMma;
+    constexpr bool kMcast = FORM == kFormMulticast;
     constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CS) - 1u);
     // bytes of one stage's W slot: half of a 256-row tile per CTA for the pair MMA
     constexpr int kWSlot = kTwoSm ? kBBytes / 2 : kBBytes;
@@ -372,7 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);  // one commit (the pair leader's when paired)
+            // one commit per stage (the pair leader's for the pair MMA), two
+            // for the multicast pair (both CTAs' MMAs read the stage's W)
+            mbar_init(&empty_bar[s], kMcast ? CS : 1);
         }
         // Only epilogue warps whose TMEM lane quarter holds live batch rows
         // take part in the tile loop and release the accumulators.
@@ -501,7 +509,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mbar_arrive_expect_tx(&full_bar[stage], bytes);
                     tma_load_2d(dA, &tmH, &full_bar[stage], kx, m * kBM, pol_h);
-                    if (tn16 == kBN) {
+                    if (kMcast) {
+                        // the stage's W is the whole tile in both CTAs; each
+                        // CTA loads half of its boxes (its 128-row half of a
+                        // whole tile, else box i when i % 2 == its rank) and
+                        // multicasts them to both
+                        if (tn16 == kBN) {
+                            tma_load_2d_multicast(dB + crank * (kBN / 2) * (kBK * 2), &tmWhalf,
+                                                  &full_bar[stage], kx,
+                                                  v0 + static_cast<int>(crank) * (kBN / 2),
+                                                  kClusterMask, pol_w);
+                        } else {
+                            for (int i = static_cast<int>(crank); i < n64 + n16; i += CS) {
+                                const int r = i < n64 ? i * 64 : n64 * 64 + (i - n64) * 16;
+                                tma_load_2d_multicast(dB + r * (kBK * 2), i < n64 ? &tmW64 : &tmW16,
+                                                      &full_bar[stage], kx, v0 + r, kClusterMask,
+                                                      pol_w);
+                            }
+                        }
+                    } else if (tn16 == kBN) {
                         // a whole tile: one box (same shared-memory layout as the
                         // 64-row boxes)
                         tma_load_2d(dB, &tmWfull, &full_bar[stage], kx, v0, pol_w);
@@ -528,7 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // its full barrier completes with parity (that number / nst) & 1.
             // A pair-MMA peer's loads complete on the leader's barriers, which
             // the leader drains (both CTAs stay resident until the cluster
-            // barrier at the end).
+            // barrier at the end).  A multicast CTA's barriers complete only
+            // once its peer's halves have landed too.
             for (int s = 0; s < nst && s < n_issued && !(kTwoSm && crank != 0); ++s) {
                 const int last = s + nst * ((n_issued - 1 - s) / nst);
                 mbar_wait_bounded(&full_bar[s], static_cast<uint32_t>(last / nst) & 1u,
@@ -590,6 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if constexpr (kTwoSm)
                         umma_commit_pair_multicast(&empty_bar[stage], kClusterMask);
+                    else if constexpr (kMcast)
+                        umma_commit_multicast(&empty_bar[stage], kClusterMask);
                     else
                         umma_commit(&empty_bar[stage]);
                     if (++stage == nst) {
@@ -727,10 +756,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (kLogprob && i < n_valid && isfinite(s)) lse_add(lse_m, lse_s, s);
                                 }
                             } else {
+                                // Both Philox blocks of the chunk first (two
+                                // independent chains for the scheduler).
+                                if (!pre_noise) {
+                                    const uint64_t v8 =
+                                        static_cast<uint64_t>(a.vocab_offset + vbase) >> 3;
+                                    noise_words8(prow, v8, xa);
+                                    if (n_valid > 8) noise_words8(prow, v8 + 1, xb);
+                                }
                                 float lt[16];
 #pragma unroll
                                 for (int i = 0; i < 16; ++i)
                                     lt[i] = __fmul_rn(__uint_as_float(r[i]), invT);
+                                // A conservative screen per element against the
+                                // best known before the chunk (a lower bound of
+                                // the running best); survivors are scanned
+                                // exactly, in order.
                                 if (kLogprob) {
                                     // online log-sum-exp over the finite l~,
                                     // rescaled once per chunk
@@ -747,22 +788,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         if (i < n_valid && isfinite(lt[i]))
                                             lse_s += exp2_approx_scaled(lt[i] - lse_m);
                                 }
-                                // A chunk whose largest l~ lies more than the
-                                // largest Gumbel below the running best holds no
-                                // winner: its noise is never drawn.  The rows of a
-                                // warp share the chunk's columns, so with peaked
-                                // logits whole warps skip it.
-                                if (first_chunk || !chunk_out_of_reach(lt, n_valid, best)) {
-                                if (!pre_noise) {
-                                    const uint64_t v8 =
-                                        static_cast<uint64_t>(a.vocab_offset + vbase) >> 3;
-                                    noise_words8(prow, v8, xa);
-                                    if (n_valid > 8) noise_words8(prow, v8 + 1, xb);
-                                }
-                                // A conservative screen per element against the
-                                // best known before the chunk (a lower bound of
-                                // the running best); survivors are scanned
-                                // exactly, in order.
                                 const float best0 = best;
                                 if (first_chunk) {
                                     // every lane's best is still -inf: all 16
@@ -804,7 +829,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     }
                                 }
                                 }  // not a first chunk
-                                }  // chunk within reach
                             }
                         }
                     } else if (row_ok) {
@@ -875,20 +899,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // before reading.  Triggering only here keeps its blocks off the SMs while
     // the epilogues run.
     griddep_launch_dependents();
-    // Pair MMA after a timeout anywhere (the device error word is set): the
-    // peer's loads complete only on the leader's barriers, and the leader
-    // drains no further than the phases it armed, so the peer gives any load
-    // still in flight a bounded 100 us to land before the pair releases its
-    // shared memory.  On the normal path every load was consumed by an MMA.
-    if (kTwoSm && crank != 0 && threadIdx.x == 0 &&
+    // Paired CTAs after a timeout anywhere (the device error word is set):
+    // a pair-MMA peer's loads complete only on the leader's barriers, and the
+    // leader drains no further than the phases it armed; a multicast CTA's
+    // drain cannot account for loads its peer issued after it stopped.  So
+    // such a CTA gives any load still in flight a bounded 100 us to land
+    // before the pair releases its shared memory.  On the normal path every
+    // load was consumed by an MMA.
+    if (((kTwoSm && crank != 0) || kMcast) && threadIdx.x == 0 &&
         *reinterpret_cast<volatile uint32_t *>(&g_status_word) != 0u) {
         const uint64_t t0 = global_timer_ns();
         while (global_timer_ns() - t0 < 100000ull) {
         }
     }
     // Paired CTAs: neither leaves while the leader's MMAs may still read the
-    // peer's shared memory or write its tensor memory, or while the peer's
-    // arrivals may still reach the leader's barriers.
+    // peer's shared memory or write its tensor memory, or while the other
+    // CTA's multicast loads, commits or arrivals may still reach it.
     if (CS > 1) cluster_sync();
     if (warp == kWarpMma) {
         __syncwarp();
@@ -899,21 +925,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int MODE, bool PAIR>
+template <int MODE, int FORM>
 static cudaError_t launch_mode(const CUtensorMap &tmH, const WMaps &wm, const Stage1Args &a,
                                int grid,
                                cudaStream_t stream) {
-    constexpr int CS = PAIR ? 2 : 1;
+    constexpr int CS = FORM == kFormSingle ? 1 : 2;
     static std::atomic<uint32_t> configured_mask{0};  // per device (device ordinals < 32)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 32 || !(configured_mask.load() & (1u << dev))) {
-        e = cudaFuncSetAttribute(stage1_kernel<MODE, PAIR>,
+        e = cudaFuncSetAttribute(stage1_kernel<MODE, FORM>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         if (CS > 1) {
-            e = cudaFuncSetAttribute(stage1_kernel<MODE, PAIR>,
+            e = cudaFuncSetAttribute(stage1_kernel<MODE, FORM>,
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
             if (e != cudaSuccess) return e;
         }
@@ -934,12 +960,14 @@ static cudaError_t launch_mode(const CUtensorMap &tmH, const WMaps &wm, const St
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, stage1_kernel<MODE, PAIR>, tmH, wm.w16, wm.w64, wm.w128,
+    return cudaLaunchKernelEx(&cfg, stage1_kernel<MODE, FORM>, tmH, wm.w16, wm.w64, wm.w128,
                               wm.w256, a);
 }
 
-// How many 2-CTA clusters of Stage 1's pair form the current device can hold
-// at once (cached per device; 0 if the query fails).
+// How many 2-CTA clusters of Stage 1's pair forms the current device can
+// hold at once (cached per device; 0 if the query fails).  Both pair forms
+// launch with the same block size and dynamic shared memory, and one block
+// fits per SM, so one query serves both.
 static int max_pair_clusters() {
     static std::mutex mu;
     static int cached[64];
@@ -949,7 +977,7 @@ static int max_pair_clusters() {
     std::lock_guard<std::mutex> lock(mu);
     if (!known[dev]) {
         int n = 0;
-        if (cudaFuncSetAttribute(stage1_kernel<kModeSample, true>,
+        if (cudaFuncSetAttribute(stage1_kernel<kModeSample, kFormPairMma>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -963,7 +991,7 @@ static int max_pair_clusters() {
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, stage1_kernel<kModeSample, true>, &cfg) !=
+            if (cudaOccupancyMaxActiveClusters(&n, stage1_kernel<kModeSample, kFormPairMma>, &cfg) !=
                 cudaSuccess)
                 n = 0;
         }
@@ -974,21 +1002,21 @@ static int max_pair_clusters() {
     return cached[dev];
 }
 
-template <bool PAIR>
+template <int FORM>
 static cudaError_t launch_form(int mode, const CUtensorMap &tmH, const WMaps &wm,
                                const Stage1Args &a, int grid, cudaStream_t stream) {
     switch (mode) {
-        case kModeSample: return launch_mode<kModeSample, PAIR>(tmH, wm, a, grid, stream);
+        case kModeSample: return launch_mode<kModeSample, FORM>(tmH, wm, a, grid, stream);
         case kModeSampleStore:
-            return launch_mode<kModeSampleStore, PAIR>(tmH, wm, a, grid, stream);
-        case kModeGemmBf16: return launch_mode<kModeGemmBf16, PAIR>(tmH, wm, a, grid, stream);
-        case kModeGemmF32: return launch_mode<kModeGemmF32, PAIR>(tmH, wm, a, grid, stream);
+            return launch_mode<kModeSampleStore, FORM>(tmH, wm, a, grid, stream);
+        case kModeGemmBf16: return launch_mode<kModeGemmBf16, FORM>(tmH, wm, a, grid, stream);
+        case kModeGemmF32: return launch_mode<kModeGemmF32, FORM>(tmH, wm, a, grid, stream);
         case kModeSampleLogprob:
-            return launch_mode<kModeSampleLogprob, PAIR>(tmH, wm, a, grid, stream);
+            return launch_mode<kModeSampleLogprob, FORM>(tmH, wm, a, grid, stream);
         case kModeSampleXform:
-            return launch_mode<kModeSampleXform, PAIR>(tmH, wm, a, grid, stream);
+            return launch_mode<kModeSampleXform, FORM>(tmH, wm, a, grid, stream);
         case kModeSampleXformLogprob:
-            return launch_mode<kModeSampleXformLogprob, PAIR>(tmH, wm, a, grid, stream);
+            return launch_mode<kModeSampleXformLogprob, FORM>(tmH, wm, a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -998,8 +1026,14 @@ cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const WMaps &wm,
                           cudaStream_t stream) {
     // Pairs only when batch tiles come in pairs and every pair fits at once.
     const bool pair = (a.nM % 2 == 0) && (2 * max_pair_clusters() >= grid);
-    if (pair) return launch_form<true>(mode, tmH, wm, a, grid, stream);
-    return launch_form<false>(mode, tmH, wm, a, grid, stream);
+    if (!pair) return launch_form<kFormSingle>(mode, tmH, wm, a, grid, stream);
+    // Measured on GB300 with the noise on (V = 128 K - 256 K): with two batch
+    // tiles the pair MMA is ahead from D = 4096 (1.5-4%) and behind at 3584
+    // (1.4%); with four it is behind at D <= 4096 (2.4-3.4%), even at 5120
+    // and ahead from 6144 (1%).
+    const int min_d = a.nM == 2 ? kPairMmaMinD2 : kPairMmaMinD;
+    if (a.D >= min_d) return launch_form<kFormPairMma>(mode, tmH, wm, a, grid, stream);
+    return launch_form<kFormMulticast>(mode, tmH, wm, a, grid, stream);
 }
 
 cudaError_t status_word_address(uint32_t **out) {

@@ -26,9 +26,10 @@
  *     returns FS_ERR_UNSUPPORTED and launches nothing.
  *   - H and W must be device memory of the current GPU (cudaMalloc-family or
  *     pool memory of that device).  Stage 1 reads them with tensor-memory
- *     loads, and in its paired form (two CTAs of a cluster sharing one MMA)
- *     both CTAs' loads complete on one CTA's barrier; those loads are kept
- *     to the calling GPU's own memory.  Page-locked host memory, another
+ *     loads, and in its paired forms (two CTAs of a cluster) a W box is
+ *     multicast to both CTAs, or both CTAs' loads complete on one CTA's
+ *     barrier to feed one MMA; those loads are kept to the calling GPU's own
+ *     memory.  Page-locked host memory, another
  *     GPU's memory (peer access) and managed memory are refused with
  *     FS_ERR_UNSUPPORTED before anything is launched.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default

@@ -1,8 +1,8 @@
 """bench.py's launcher logic, on CPU.
 
 The fused sampling path runs on one GPU: it does not shard, and Stage 1's
-paired kernel couples the two CTAs of a cluster (one MMA over both), which
-is kept to single-GPU runs.  So the GPU arm refuses --gpus N > 1 and torchrun worlds
+paired forms couple the two CTAs of a cluster (multicast W loads or one MMA
+over both), which are kept to single-GPU runs.  So the GPU arm refuses --gpus N > 1 and torchrun worlds
 larger than one (exit status 2, before touching a device), while the
 reference arm (the CPU oracle) runs on rank 0 only and the other ranks exit
 without work.

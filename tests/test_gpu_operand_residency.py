@@ -1,7 +1,7 @@
 """Stage 1 reads H and W only from the calling GPU's own memory.
 
 Its TMA tensor maps are encoded on the caller's pointers, and in the paired
-kernel both CTAs of a cluster feed one MMA.  The entry points
+forms both CTAs of a cluster share W boxes (multicast) or feed one MMA.  The entry points
 check where H and W live before encoding anything: page-locked host memory
 (reachable through a mapping) and pageable host memory are refused with
 FS_ERR_UNSUPPORTED, nothing is launched, and the outputs stay untouched.
@@ -31,7 +31,7 @@ def _stream():
 @pytest.mark.parametrize("where", ["pinned", "pageable"])
 @pytest.mark.parametrize("operand", ["W", "H"])
 def test_host_operands_are_refused(fs, where, operand):
-    B, V, D = 256, 4096, 64  # B = 256: the paired kernel's shape
+    B, V, D = 256, 4096, 64  # B = 256: a paired shape
     dev = torch.device("cuda:0")
     H = torch.zeros((B, D), dtype=torch.bfloat16, device=dev)
     W = torch.zeros((V, D), dtype=torch.bfloat16, device=dev)

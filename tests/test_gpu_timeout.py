@@ -27,7 +27,8 @@ import exact_sampling_lm_gb300 as fs
 from exact_sampling_lm_gb300 import _lib
 torch.cuda.set_device(0)
 g = torch.Generator(device="cpu").manual_seed(1)
-for B, V, D in ((4, 4096, 256), (256, 20000, 64)):  # unpaired and 2-CTA-cluster launches
+# one CTA per batch tile, the multicast pair, the pair MMA
+for B, V, D in ((4, 4096, 256), (256, 20000, 64), (256, 3000, 6144)):
     H = torch.randn((B, D), generator=g).to(torch.bfloat16).cuda()
     W = (torch.randn((V, D), generator=g) * 0.1).to(torch.bfloat16).cuda()
     ws = fs.workspace(B, V, D)
@@ -62,4 +63,4 @@ def test_bounded_wait_expires_and_reports_timeout():
                          env=env, timeout=300)
     print(res.stdout)
     assert res.returncode == 0, res.stderr[-2000:]
-    assert res.stdout.count("timeout path ok") == 2
+    assert res.stdout.count("timeout path ok") == 3
