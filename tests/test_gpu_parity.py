@@ -172,6 +172,42 @@ def test_ragged_shapes(fs, dev, B, V, D):
     run_and_check(fs, H, W, 0.9, 1000 + B, 3, "B=%d V=%d D=%d" % (B, V, D))
 
 
+def _random_shapes(n=48, seed=20261203):
+    """Seeded (B, V, D) triples spread over the three launch forms: one batch
+    tile, an odd number of batch tiles (unpaired), two and four batch tiles
+    (paired: the multicast pair below the D switch, the pair MMA above it;
+    half of the paired draws take D in 3584..8192).  D is a multiple of 8 (the call's own rule), V x D stays below 3e7 so
+    that the oracle's rows take well under a second."""
+    rng = np.random.default_rng(seed)
+    spans = [(1, 128), (129, 256), (257, 384), (385, 512)]
+    out = []
+    for k in range(n):
+        lo, hi = spans[k % len(spans)]
+        B = int(rng.integers(lo, hi + 1))
+        if k % 4 in (1, 3) and k % 8 >= 4:  # paired, near and above the form switch
+            D = 8 * int(rng.integers(448, 1025))
+        else:
+            D = int(8 * max(1, round(float(np.exp(rng.uniform(0.0, np.log(1024)))))))
+        vmax = max(1, min(60000, int(3e7 // D)))
+        V = int(max(1, round(float(np.exp(rng.uniform(0.0, np.log(vmax)))))))
+        out.append((B, V, D))
+    return out
+
+
+@pytest.mark.parametrize("k,B,V,D", [(k,) + s for k, s in enumerate(_random_shapes())])
+def test_seeded_random_shapes(fs, dev, k, B, V, D):
+    """Random shapes from a fixed seed: six rows (first, last, spread) of each
+    against the oracle, alternately in the logits-store mode (logits compared
+    too) and in the plain sampling mode, with a scalar or a per-row
+    temperature."""
+    g = torch.Generator(device="cpu").manual_seed(7000 + k)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * (2.0 / D ** 0.5)).to(torch.bfloat16).to(dev)
+    T = (0.3 + 1.2 * torch.rand(B, generator=g)).to(dev) if k % 3 == 0 else 0.3 + 0.1 * (k % 12)
+    run_and_check(fs, H, W, T, 500 + k, k, "random k=%d B=%d V=%d D=%d" % (k, B, V, D),
+                  store=(k % 2 == 0), rows=spread_rows(B, 6))
+
+
 @pytest.mark.parametrize("B,V,D,T,spread", [(64, 50000, 64, 0.05, 1.0), (200, 60000, 128, 1.0, 12.0),
                                              (256, 151936, 64, 0.8, 8.0), (3, 20011, 64, 0.01, 1.0)])
 def test_peaked_logits(fs, dev, B, V, D, T, spread):
