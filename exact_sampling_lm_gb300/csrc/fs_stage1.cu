@@ -31,7 +31,11 @@
 //               running per-row argmax across all tiles of the CTA.  The
 //               epilogue of tile t overlaps the MMA of tile t+1 (double-buffered
 //               TMEM).  At the end the column parts of each row are
-//               merged through shared memory.
+//               merged through shared memory.  In the pair MMA, warps 14
+//               and 15 instead sample the last column part of lane quarters
+//               0 and 1, from raw logits that warps 0 and 1 pass through a
+//               shared-memory ring, so that the sub-partitions of the TMA
+//               producer and the MMA issuer carry less of the epilogue.
 // Batch rows sit on the MMA M dimension, so each epilogue thread owns one row
 // and scans its columns in increasing order: the lowest-index tie rule and
 // the 8-wide Philox block both fall out without cross-lane exchange.
@@ -74,6 +78,16 @@ constexpr uint32_t kStatusTimeout = 1u;
 constexpr int kFormSingle = 0;
 constexpr int kFormMulticast = 1;
 constexpr int kFormPairMma = 2;
+// Column hand-off ring (see the epilogue): per lane quarter 0 and 1,
+// kExpSlots chunks of 16 columns x 32 rows of raw f32 logits, stored
+// element-major (element i of lane l at i * 32 + l: conflict-free), after a
+// 128-byte block of its full / empty barriers.
+constexpr int kExpSlots = 4;
+constexpr int kExpChunkFloats = 16 * 32;
+constexpr int kExportBytes = 128 + 2 * kExpSlots * kExpChunkFloats * 4;
+static_assert(4 * kExpSlots * 8 <= 128, "hand-off barriers");
+// room behind the pair MMA's operand ring (6 stages of 32 KB)
+static_assert(kRingBytes - 6 * (kABytes + kBBytes / 2) >= kExportBytes, "hand-off ring");
 // the pair MMA serves paired calls with D at least this: with two batch
 // tiles, or with more
 constexpr int kPairMmaMinD2 = 4096;
@@ -284,6 +298,131 @@ __device__ __forceinline__ void store_bf16_chunk(__nv_bfloat16 *dst, int n,
     }
 }
 
+// Running state of one sampled row in one epilogue thread: the best perturbed
+// score and its index, and (log-probability modes) the log-mass of the
+// elements seen, lse_m = max l~, lse_s = sum exp(l~ - lse_m), with best_lt =
+// l~ of the best.
+struct SampleRow {
+    float best, lse_m, lse_s, best_lt, invT;
+    int bidx, b;
+    bool row_ok, t_ok;
+    PhiloxRow prow;
+};
+
+__device__ __forceinline__ SampleRow sample_row(const Stage1Args &a, bool sampling, int b,
+                                                bool row_ok) {
+    SampleRow s;
+    s.best = -INFINITY;
+    s.bidx = -1;
+    s.lse_m = -INFINITY;
+    s.lse_s = 0.0f;
+    s.best_lt = NAN;
+    s.invT = 0.0f;
+    s.t_ok = false;
+    s.b = b;
+    s.row_ok = row_ok;
+    if (sampling && row_ok) {
+        const float T = a.temps ? a.temps[b] : a.temp_scalar;
+        s.t_ok = isfinite(T) && T > 0.0f;
+        s.invT = __frcp_rn(T);
+    }
+    s.prow = philox_row(a.seed, a.offset, static_cast<uint64_t>(b));
+    return s;
+}
+
+// One 16-column chunk of one row (raw f32 accumulator bits r, columns vbase ..
+// vbase + n_valid - 1 of the partition's vocabulary): optional logits store and
+// transforms, s = l * (1/T) + g with g from the Philox words (drawn here unless
+// have_words), and the running best.  first_chunk is a warp-wide vote taken
+// by the caller: every lane's best is still -inf.
+template <int MODE>
+__device__ __forceinline__ void sample_chunk(const Stage1Args &a, SampleRow &st,
+                                             uint32_t (&r)[16], int vbase, int n_valid,
+                                             bool first_chunk, bool have_words,
+                                             uint32_t (&xa)[8], uint32_t (&xb)[8]) {
+    constexpr bool kLogprob = (MODE == kModeSampleLogprob || MODE == kModeSampleXformLogprob);
+    constexpr bool kXform = (MODE == kModeSampleXform || MODE == kModeSampleXformLogprob);
+    if (MODE == kModeSampleStore && st.row_ok)
+        store_f32_chunk(a.out_logits + static_cast<size_t>(st.b) * a.V + vbase, n_valid, r,
+                        a.y_vec_ok != 0);
+    if (kXform && st.row_ok && st.t_ok) apply_transforms(a, st.b, vbase, n_valid, r);
+    if (!(st.row_ok && st.t_ok)) return;
+    if (a.flags & 1u) {  // noise off
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float s = __fmul_rn(__uint_as_float(r[i]), st.invT);
+            if (i < n_valid && s > st.best) {
+                st.best = s;
+                st.bidx = static_cast<int>(a.vocab_offset) + vbase + i;
+                st.best_lt = s;
+            }
+            if (kLogprob && i < n_valid && isfinite(s)) lse_add(st.lse_m, st.lse_s, s);
+        }
+        return;
+    }
+    // Both Philox blocks of the chunk first (two independent chains for the
+    // scheduler).
+    if (!have_words) {
+        const uint64_t v8 = static_cast<uint64_t>(a.vocab_offset + vbase) >> 3;
+        noise_words8(st.prow, v8, xa);
+        if (n_valid > 8) noise_words8(st.prow, v8 + 1, xb);
+    }
+    float lt[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) lt[i] = __fmul_rn(__uint_as_float(r[i]), st.invT);
+    if (kLogprob) {
+        // online log-sum-exp over the finite l~, rescaled once per chunk
+        float cm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i < n_valid && isfinite(lt[i])) cm = fmaxf(cm, lt[i]);
+        if (cm > st.lse_m) {
+            st.lse_s *= exp2_approx_scaled(st.lse_m - cm);
+            st.lse_m = cm;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i < n_valid && isfinite(lt[i])) st.lse_s += exp2_approx_scaled(lt[i] - st.lse_m);
+    }
+    if (first_chunk) {
+        // every lane's best is still -inf: all 16 elements would survive the
+        // screen, so score them directly
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t xi = i < 8 ? xa[i] : xb[i - 8];
+            const float s = __fadd_rn(lt[i], gumbel_from_word(xi));
+            if (i < n_valid && s > st.best) {
+                st.best = s;
+                st.bidx = static_cast<int>(a.vocab_offset) + vbase + i;
+                if (kLogprob) st.best_lt = lt[i];
+            }
+        }
+        return;
+    }
+    // A conservative screen per element against the best known before the
+    // chunk (a lower bound of the running best); survivors are scored
+    // exactly, lowest index first (keeps the tie rule).  A loop over the set
+    // bits costs one iteration per survivor instead of a predicated
+    // evaluation of every element.
+    const float best0 = st.best;
+    uint32_t pass = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t xi = i < 8 ? xa[i] : xb[i - 8];
+        if (i < n_valid && screen_lg2_tail(xi) < screen_bound(lt[i], best0)) pass |= 1u << i;
+    }
+    while (pass) {
+        const int i = __ffs(pass) - 1;
+        pass &= pass - 1;
+        const float s = __fadd_rn(pick16(lt, i), gumbel_from_word(pick16x(xa, xb, i)));
+        if (s > st.best) {
+            st.best = s;
+            st.bidx = static_cast<int>(a.vocab_offset) + vbase + i;
+            if (kLogprob) st.best_lt = pick16(lt, i);
+        }
+    }
+}
+
 }  // namespace
 
 // FORM selects the launch form.
@@ -318,7 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                               MODE == kModeSampleLogprob || MODE == kModeSampleXform ||
                               MODE == kModeSampleXformLogprob);
     constexpr bool kLogprob = (MODE == kModeSampleLogprob || MODE == kModeSampleXformLogprob);
-    constexpr bool kXform = (MODE == kModeSampleXform || MODE == kModeSampleXformLogprob);
     constexpr int CS = FORM == kFormSingle ? 1 : 2;  // CTAs per cluster
     constexpr bool kTwoSm = FORM == kFormPairMma;
     constexpr bool kMcast = FORM == kFormMulticast;
@@ -347,6 +485,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane_off = (a.nM != 1) ? 0 : (a.B <= 64 ? 64 : (a.B <= 96 ? 32 : 0));
     uint8_t *sA = smem + kPreRingBytes;
     uint8_t *sB = sA + nst * a_stride;
+    // Column hand-off (sampling modes of the pair MMA): behind the operand
+    // ring.  Measured: 1-2% faster for the pair MMA at D = 3584-8192; the
+    // multicast pair at D = 2304 was 4% slower with it (there the epilogue
+    // fills most of each tile's MMA time on every sub-partition), so it
+    // runs without.
+    uint8_t *sX = sB + nst * kWSlot;
+    const bool exp_on = kSample && kTwoSm &&
+                        kRingBytes - nst * (a_stride + kWSlot) >= kExportBytes;
+    uint64_t *exp_full = reinterpret_cast<uint64_t *>(sX);  // [2][kExpSlots]
+    uint64_t *exp_empty = exp_full + 2 * kExpSlots;         // [2][kExpSlots]
+    float *exp_ring = reinterpret_cast<float *>(sX + 128);   // [2][kExpSlots][16][32]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     uint64_t *full_bar = bars;
     uint64_t *empty_bar = bars + kMaxStages;
@@ -383,12 +532,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty_bar[s], kMcast ? CS : 1);
         }
         // Only epilogue warps whose TMEM lane quarter holds live batch rows
-        // take part in the tile loop and release the accumulators.
+        // take part in the tile loop and release the accumulators (with the
+        // column hand-off, three per quarter: warps 14 and 15 read no tensor
+        // memory).
         auto live_warps = [&](int mt) {
             int n = 0;
             for (int qq = 0; qq < 4; ++qq)
                 if (qq * 32 >= lane_off && (mt * kBM + qq * 32 - lane_off) < a.B)
-                    n += quarter_parts(qq);
+                    n += exp_on ? 3 : quarter_parts(qq);
             return n;
         };
         for (int i = 0; i < 2; ++i) {
@@ -399,6 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&tempty_peer[i], kTwoSm ? max(1, live_warps(m + 1)) : 1);
         }
         mbar_init(done_bar, 1);
+        if (exp_on)
+            for (int i = 0; i < 2 * kExpSlots; ++i) {
+                mbar_init(&exp_full[i], 32);   // every lane of the passing warp
+                mbar_init(&exp_empty[i], 32);  // every lane of the receiving warp
+            }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -644,31 +800,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------ epilogue warps
         const int q = warp & 3;   // TMEM lane quarter (the warp's rank in its warpgroup)
-        const int j = warp < 12 ? (warp >> 2) : 3;  // column part of the tile (warps 14, 15: 3)
-        const int np = quarter_parts(q);
-        const int tl = q * 32 + lane;  // TMEM lane = accumulator row
-        const int row = tl - lane_off;  // row within the batch tile
+        // Roles.  Without the column hand-off, warp w reads lane quarter q =
+        // w % 4 and takes column part w / 4 of quarter_parts(q) (warps 14 and
+        // 15: part 3).  With it, warps 0-11 take parts 0-2: of four parts in
+        // quarters 0 and 1 and of three in quarters 2 and 3.  Part 3 of
+        // quarters 0 and 1 is sampled by warps 14 and 15 on sub-partitions 2
+        // and 3, from the raw logits that warps 0 and 1 pass through the
+        // hand-off ring, so that sub-partitions 0 and 1 (TMA producer, MMA
+        // issuer) carry less of the epilogue.
+        const bool importer = exp_on && warp >= 14;
+        const int j = warp < 12 ? (warp >> 2) : 3;  // column part of the tile
+        const int np = exp_on ? (q < 2 ? 4 : 3) : quarter_parts(q);
+        const int rq = importer ? q - 2 : q;  // lane quarter of the rows this warp samples
+        const int tl = rq * 32 + lane;        // accumulator row
+        const int row = tl - lane_off;        // row within the batch tile
         const int b = m * kBM + row;
-        const bool warp_has_rows = q * 32 >= lane_off && (m * kBM + q * 32 - lane_off) < a.B;
-        const bool row_ok = row >= 0 && b < a.B;
-        float invT = 0.0f;
-        bool t_ok = false;
-        if (kSample && row_ok) {
-            const float T = a.temps ? a.temps[b] : a.temp_scalar;
-            t_ok = isfinite(T) && T > 0.0f;
-            invT = __frcp_rn(T);
-        }
+        const bool quarter_live = rq * 32 >= lane_off && (m * kBM + rq * 32 - lane_off) < a.B;
+        const bool reads_tmem = !importer && quarter_live;
+        const bool exporter = exp_on && !importer && q < 2 && j == 0 && quarter_live;
+        SampleRow st = sample_row(a, kSample, b, row >= 0 && b < a.B);
         const bool no_noise = (a.flags & 1u) != 0;
-        const PhiloxRow prow = philox_row(a.seed, a.offset, static_cast<uint64_t>(b));
-        float best = -INFINITY;
-        int bidx = -1;
-        // log-mass of the row's elements seen by this thread (kLogprob):
-        // lse_m = max l~, lse_s = sum exp(l~ - lse_m); best_lt = l~ of the best
-        float lse_m = -INFINITY, lse_s = 0.0f, best_lt = NAN;
         bool ok = true;
+        int xcnt = 0;  // chunks passed through the hand-off ring so far
         // Warps without live rows skip the tile loop (they are not counted by
         // the accumulator-release barrier) and wait at the combine barrier.
-        for (int t = 0; t < (warp_has_rows ? ntiles : 0); ++t) {
+        for (int t = 0; t < (reads_tmem ? ntiles : 0); ++t) {
             const int acc = t & 1;
             const uint32_t aphase = static_cast<uint32_t>(t >> 1) & 1u;
             // The last tile's epilogue is the one no MMA hides.  Its noise
@@ -692,8 +848,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c0 = lo; c0 < hi; c0 += 16) {
                     uint32_t wa[8], wb[8], w[16];
                     const uint64_t v8 = static_cast<uint64_t>(a.vocab_offset + v0p + c0) >> 3;
-                    noise_words8(prow, v8, wa);
-                    noise_words8(prow, v8 + 1, wb);
+                    noise_words8(st.prow, v8, wa);
+                    noise_words8(st.prow, v8 + 1, wb);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         w[i] = wa[i];
@@ -711,136 +867,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             int v0, tn;
             tile_geom(geom, t, v0, tn);
-            const int c_lo = col_part_start(j, tn, np);
-            const int c_hi = col_part_start(j + 1, tn, np);
-            {
-                for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+            if (exporter) {
+                // part 3 of this quarter's rows, raw, into the hand-off ring
+                uint64_t *xfull = exp_full + q * kExpSlots;
+                uint64_t *xempty = exp_empty + q * kExpSlots;
+                for (int c0 = col_part_start(3, tn, 4); c0 < tn; c0 += 16, ++xcnt) {
+                    const int slot = xcnt % kExpSlots;
+                    if (!mbar_wait_bounded_backoff(&xempty[slot],
+                                                   (static_cast<uint32_t>(xcnt / kExpSlots) & 1u) ^ 1u,
+                                                   a.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    __syncwarp();
                     uint32_t r[16];
                     tmem_ld16_wait(tmem_base + static_cast<uint32_t>(acc * kBN + c0) +
                                        (static_cast<uint32_t>(q * 32) << 16),
                                    r);
-                    // the parked noise of the last tile, read by the whole (converged) warp
-                    uint32_t xa[8], xb[8];
-                    if (pre_noise) {
-                        uint32_t w[16];
-                        tmem_ld16_wait(tmem_base + static_cast<uint32_t>((acc ^ 1) * kBN + c0) +
-                                           (static_cast<uint32_t>(q * 32) << 16),
-                                       w);
+                    float *dst = exp_ring + (q * kExpSlots + slot) * kExpChunkFloats;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            xa[i] = w[i];
-                            xb[i] = w[8 + i];
-                        }
+                    for (int i = 0; i < 16; ++i) dst[i * 32 + lane] = __uint_as_float(r[i]);
+                    mbar_arrive(&xfull[slot]);  // each lane: its own stores are released
+                }
+                if (!ok) break;
+            }
+            const int c_lo = col_part_start(j, tn, np);
+            const int c_hi = col_part_start(j + 1, tn, np);
+            for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16_wait(tmem_base + static_cast<uint32_t>(acc * kBN + c0) +
+                                   (static_cast<uint32_t>(q * 32) << 16),
+                               r);
+                // the parked noise of the last tile, read by the whole (converged) warp
+                uint32_t xa[8], xb[8];
+                if (pre_noise) {
+                    uint32_t w[16];
+                    tmem_ld16_wait(tmem_base + static_cast<uint32_t>((acc ^ 1) * kBN + c0) +
+                                       (static_cast<uint32_t>(q * 32) << 16),
+                                   w);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        xa[i] = w[i];
+                        xb[i] = w[8 + i];
                     }
-                    const int n_valid = min(16, c_hi - c0);
-                    const int vbase = v0 + c0;
+                }
+                const int n_valid = min(16, c_hi - c0);
+                const int vbase = v0 + c0;
+                if (kSample) {
                     // warp-wide vote while the warp is converged; lanes without
                     // a live row keep best = -inf and never block it
-                    const bool first_chunk = __all_sync(0xffffffffu, best == -INFINITY);
-                    if (kSample) {
-                        if (MODE == kModeSampleStore && row_ok)
-                            store_f32_chunk(a.out_logits + static_cast<size_t>(b) * a.V + vbase,
-                                            n_valid, r, a.y_vec_ok != 0);
-                        if (kXform && row_ok && t_ok)
-                            apply_transforms(a, b, vbase, n_valid, r);
-                        if (row_ok && t_ok) {
-                            if (no_noise) {
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    const float s = __fmul_rn(__uint_as_float(r[i]), invT);
-                                    if (i < n_valid && s > best) {
-                                        best = s;
-                                        bidx = static_cast<int>(a.vocab_offset) + vbase + i;
-                                        best_lt = s;
-                                    }
-                                    if (kLogprob && i < n_valid && isfinite(s)) lse_add(lse_m, lse_s, s);
-                                }
-                            } else {
-                                // Both Philox blocks of the chunk first (two
-                                // independent chains for the scheduler).
-                                if (!pre_noise) {
-                                    const uint64_t v8 =
-                                        static_cast<uint64_t>(a.vocab_offset + vbase) >> 3;
-                                    noise_words8(prow, v8, xa);
-                                    if (n_valid > 8) noise_words8(prow, v8 + 1, xb);
-                                }
-                                float lt[16];
-#pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    lt[i] = __fmul_rn(__uint_as_float(r[i]), invT);
-                                // A conservative screen per element against the
-                                // best known before the chunk (a lower bound of
-                                // the running best); survivors are scanned
-                                // exactly, in order.
-                                if (kLogprob) {
-                                    // online log-sum-exp over the finite l~,
-                                    // rescaled once per chunk
-                                    float cm = -INFINITY;
-#pragma unroll
-                                    for (int i = 0; i < 16; ++i)
-                                        if (i < n_valid && isfinite(lt[i])) cm = fmaxf(cm, lt[i]);
-                                    if (cm > lse_m) {
-                                        lse_s *= exp2_approx_scaled(lse_m - cm);
-                                        lse_m = cm;
-                                    }
-#pragma unroll
-                                    for (int i = 0; i < 16; ++i)
-                                        if (i < n_valid && isfinite(lt[i]))
-                                            lse_s += exp2_approx_scaled(lt[i] - lse_m);
-                                }
-                                const float best0 = best;
-                                if (first_chunk) {
-                                    // every lane's best is still -inf: all 16
-                                    // elements would survive the screen, so
-                                    // score them directly
-#pragma unroll
-                                    for (int i = 0; i < 16; ++i) {
-                                        const uint32_t xi = i < 8 ? xa[i] : xb[i - 8];
-                                        const float s = __fadd_rn(lt[i], gumbel_from_word(xi));
-                                        if (i < n_valid && s > best) {
-                                            best = s;
-                                            bidx = static_cast<int>(a.vocab_offset) + vbase + i;
-                                            if (kLogprob) best_lt = lt[i];
-                                        }
-                                    }
-                                } else {
-                                uint32_t pass = 0;
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    const uint32_t xi = i < 8 ? xa[i] : xb[i - 8];
-                                    if (i < n_valid &&
-                                        screen_lg2_tail(xi) < screen_bound(lt[i], best0))
-                                        pass |= 1u << i;
-                                }
-                                // Exact scores only for the survivors, lowest
-                                // index first (keeps the tie rule).  A loop over
-                                // the set bits costs one iteration per survivor
-                                // instead of a predicated evaluation of every
-                                // element.
-                                while (pass) {
-                                    const int i = __ffs(pass) - 1;
-                                    pass &= pass - 1;
-                                    const float s =
-                                        __fadd_rn(pick16(lt, i), gumbel_from_word(pick16x(xa, xb, i)));
-                                    if (s > best) {
-                                        best = s;
-                                        bidx = static_cast<int>(a.vocab_offset) + vbase + i;
-                                        if (kLogprob) best_lt = pick16(lt, i);
-                                    }
-                                }
-                                }  // not a first chunk
-                            }
-                        }
-                    } else if (row_ok) {
-                        if (MODE == kModeGemmF32)
-                            store_f32_chunk(static_cast<float *>(a.out_y) +
-                                                static_cast<size_t>(b) * a.V + vbase,
-                                            n_valid, r, a.y_vec_ok != 0);
-                        else
-                            store_bf16_chunk(static_cast<__nv_bfloat16 *>(a.out_y) +
-                                                 static_cast<size_t>(b) * a.V + vbase,
-                                             n_valid, r, a.y_vec_ok != 0);
-                    }
+                    const bool first_chunk = __all_sync(0xffffffffu, st.best == -INFINITY);
+                    sample_chunk<MODE>(a, st, r, vbase, n_valid, first_chunk, pre_noise, xa, xb);
+                } else if (st.row_ok) {
+                    if (MODE == kModeGemmF32)
+                        store_f32_chunk(static_cast<float *>(a.out_y) +
+                                            static_cast<size_t>(b) * a.V + vbase,
+                                        n_valid, r, a.y_vec_ok != 0);
+                    else
+                        store_bf16_chunk(static_cast<__nv_bfloat16 *>(a.out_y) +
+                                             static_cast<size_t>(b) * a.V + vbase,
+                                         n_valid, r, a.y_vec_ok != 0);
                 }
             }
             tc_fence_before_sync();
@@ -853,19 +939,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_peer[acc]), 0u));
             }
         }
+        // Warps 14 and 15 with the hand-off: part 3 of quarter 0 or 1, chunk
+        // by chunk as the ring fills.  They never touch tensor memory, so the
+        // accumulators are released without them.
+        if (kSample && importer && quarter_live) {
+            uint64_t *xfull = exp_full + rq * kExpSlots;
+            uint64_t *xempty = exp_empty + rq * kExpSlots;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                int v0, tn;
+                tile_geom(geom, t, v0, tn);
+                for (int c0 = col_part_start(3, tn, 4); c0 < tn; c0 += 16, ++xcnt) {
+                    const int slot = xcnt % kExpSlots;
+                    if (!mbar_wait_bounded_backoff(&xfull[slot],
+                                                   static_cast<uint32_t>(xcnt / kExpSlots) & 1u,
+                                                   a.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    __syncwarp();
+                    uint32_t r[16];
+                    const float *src = exp_ring + (rq * kExpSlots + slot) * kExpChunkFloats;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(src[i * 32 + lane]);
+                    mbar_arrive(&xempty[slot]);  // each lane, after its loads
+                    const bool first_chunk = __all_sync(0xffffffffu, st.best == -INFINITY);
+                    uint32_t xa[8], xb[8];
+                    sample_chunk<MODE>(a, st, r, v0 + c0, min(16, tn - c0), first_chunk, false,
+                                       xa, xb);
+                }
+            }
+        }
         if (!ok) raise_timeout(abort_flag);
         if (kSample) {
             // Combine the column parts' bests of each row (tie: lower index),
             // then one candidate per (row, partition).
-            comb_s[j * kBM + tl] = best;
-            comb_i[j * kBM + tl] = bidx;
+            comb_s[j * kBM + tl] = st.best;
+            comb_i[j * kBM + tl] = st.bidx;
             if (kLogprob) {
-                comb_lt[j * kBM + tl] = best_lt;
-                comb_m[j * kBM + tl] = lse_m;
-                comb_sum[j * kBM + tl] = lse_s;
+                comb_lt[j * kBM + tl] = st.best_lt;
+                comb_m[j * kBM + tl] = st.lse_m;
+                comb_sum[j * kBM + tl] = st.lse_s;
             }
             epilogue_barrier();
-            if (j == 0 && row_ok) {
+            if (j == 0 && st.row_ok) {
+                float best = st.best, best_lt = st.best_lt, lse_m = st.lse_m, lse_s = st.lse_s;
+                int bidx = st.bidx;
 #pragma unroll
                 for (int jj = 1; jj < np; ++jj) {
                     const float s = comb_s[jj * kBM + tl];
