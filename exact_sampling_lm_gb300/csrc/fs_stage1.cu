@@ -445,8 +445,8 @@ __device__ __forceinline__ void sample_chunk(const Stage1Args &a, SampleRow &st,
 //      accumulator once both CTAs' epilogue warps have released it (the
 //      peer's warps arrive remotely on the leader's tempty_peer, once per
 //      tile).
-//   Both pair forms move the same bytes; which is faster depends on D (see
-//   launch_stage1).
+//   Both pair forms move the same bytes from L2; which is faster depends on
+//   D and on the number of batch tiles (see launch_stage1).
 template <int MODE, int FORM>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW16,
