@@ -28,6 +28,12 @@ FS_FLAG_NO_NOISE = 0x1
 FS_FLAG_STORE_LOGITS = 0x2
 FS_DTYPE_BF16 = 0
 FS_DTYPE_F32 = 1
+# Stage 1 launch forms (fs_stage1_form)
+FS_STAGE1_ONE_CTA = 0
+FS_STAGE1_MULTICAST_PAIR = 1
+FS_STAGE1_PAIR_MMA = 2
+STAGE1_FORM_NAMES = {FS_STAGE1_ONE_CTA: "one CTA per tile", FS_STAGE1_MULTICAST_PAIR: "multicast pair",
+                     FS_STAGE1_PAIR_MMA: "pair MMA"}
 
 
 class Transforms(ctypes.Structure):
@@ -74,6 +80,7 @@ SIGNATURES = {
     "fs_debug_gumbel": ([_vp, _i64, _vp, _vp], _int),
     "fs_get_device_status": ([_vp, ctypes.POINTER(_u32)], _int),
     "fs_plan_info": ([_i64, _i64, _i64, _int, ctypes.POINTER(_i64)], _int),
+    "fs_stage1_form": ([_i64, _i64, _i64, ctypes.POINTER(_int)], _int),
     "fs_release_workspaces": ([], _int),
     "fs_sample_noalloc": ([_vp, _vp, _i64, _i64, _i64, _f32, _vp, _u64, _u64, _vp, _vp, _vp], _int),
     "fs_last_error_string": ([], ctypes.c_char_p),
@@ -153,6 +160,13 @@ def fs_plan_info(B: int, V: int, D: int, num_sms: int) -> dict:
     _check(lib().fs_plan_info(B, V, D, num_sms, out))
     keys = ("nM", "P", "G", "nCand", "ws_bytes", "max_tiles")
     return {k: int(v) for k, v in zip(keys, out)}
+
+
+def fs_stage1_form(B: int, V: int, D: int) -> int:
+    """The Stage 1 launch form (FS_STAGE1_*) for (B, V, D) on the current GPU."""
+    out = _int(0)
+    _check(lib().fs_stage1_form(B, V, D, ctypes.byref(out)))
+    return int(out.value)
 
 
 def fs_workspace_size(B: int, V: int, D: int) -> int:

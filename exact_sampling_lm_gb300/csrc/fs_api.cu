@@ -497,6 +497,19 @@ fs_status fs_plan_info(int64_t B, int64_t V, int64_t D, int num_sms, int64_t out
     return FS_OK;
 }
 
+fs_status fs_stage1_form(int64_t B, int64_t V, int64_t D, int *out_form) {
+    if (!out_form) return fail(FS_ERR_INVALID_ARG, "out_form must be non-null");
+    fs_status st = validate_shape(B, V, D);
+    if (st != FS_OK) return st;
+    int dev = 0;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != FS_OK) return st;
+    Plan p;
+    make_plan(B, V, D, info.sms, &p);
+    *out_form = stage1_form(static_cast<int>(p.nM), static_cast<int>(D), static_cast<int>(p.G));
+    return FS_OK;
+}
+
 }  // extern "C"
 
 namespace fs {

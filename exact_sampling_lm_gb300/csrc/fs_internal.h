@@ -124,6 +124,9 @@ struct WMaps {
 cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const WMaps &wm,
                           const Stage1Args &a, int grid,
                           cudaStream_t stream);
+// The launch form launch_stage1 takes on the current device for nM batch
+// tiles, depth D and `grid` CTAs (FS_STAGE1_* of fs_sample.h).
+int stage1_form(int nM, int D, int grid);
 
 // Stage 2 reads Stage 1's device error word (status_word_address): while it
 // is set, every row gets out_idx = -1 and NaN scores, so a call whose Stage 1

@@ -1139,19 +1139,26 @@ static cudaError_t launch_form(int mode, const CUtensorMap &tmH, const WMaps &wm
     }
 }
 
-cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const WMaps &wm,
-                          const Stage1Args &a, int grid,
-                          cudaStream_t stream) {
+int stage1_form(int nM, int D, int grid) {
     // Pairs only when batch tiles come in pairs and every pair fits at once.
-    const bool pair = (a.nM % 2 == 0) && (2 * max_pair_clusters() >= grid);
-    if (!pair) return launch_form<kFormSingle>(mode, tmH, wm, a, grid, stream);
+    const bool pair = (nM % 2 == 0) && (2 * max_pair_clusters() >= grid);
+    if (!pair) return kFormSingle;
     // Measured on GB300 with the noise on (V = 128 K - 256 K): with two batch
     // tiles the pair MMA is ahead from D = 4096 (1.5-4%) and behind at 3584
     // (1.4%); with four it is behind at D <= 4096 (2.4-3.4%), even at 5120
     // and ahead from 6144 (1%).
-    const int min_d = a.nM == 2 ? kPairMmaMinD2 : kPairMmaMinD;
-    if (a.D >= min_d) return launch_form<kFormPairMma>(mode, tmH, wm, a, grid, stream);
-    return launch_form<kFormMulticast>(mode, tmH, wm, a, grid, stream);
+    const int min_d = nM == 2 ? kPairMmaMinD2 : kPairMmaMinD;
+    return D >= min_d ? kFormPairMma : kFormMulticast;
+}
+
+cudaError_t launch_stage1(int mode, const CUtensorMap &tmH, const WMaps &wm,
+                          const Stage1Args &a, int grid,
+                          cudaStream_t stream) {
+    switch (stage1_form(a.nM, a.D, grid)) {
+        case kFormPairMma: return launch_form<kFormPairMma>(mode, tmH, wm, a, grid, stream);
+        case kFormMulticast: return launch_form<kFormMulticast>(mode, tmH, wm, a, grid, stream);
+        default: return launch_form<kFormSingle>(mode, tmH, wm, a, grid, stream);
+    }
 }
 
 cudaError_t status_word_address(uint32_t **out) {

@@ -350,6 +350,28 @@ fs_status fs_get_device_status(void *stream, uint32_t *out_word);
 fs_status fs_plan_info(int64_t B, int64_t V, int64_t D, int num_sms, int64_t out[6]);
 
 /* ---------------------------------------------------------------------------
+ * fs_stage1_form -- which form of Stage 1 (method section: one batch tile x
+ * one vocabulary tile per step, here in one of three launch forms) the
+ * sampling and GEMM entry points launch for (B, V, D) on the current GPU.
+ * Launches nothing; the first call per device queries how many 2-CTA
+ * clusters fit at once.
+ *   FS_STAGE1_ONE_CTA          one CTA per (batch tile, vocabulary partition):
+ *                              one or an odd number of 128-row batch tiles,
+ *                              or pairs that would not all fit at once
+ *   FS_STAGE1_MULTICAST_PAIR   2-CTA clusters over two batch tiles, each CTA
+ *                              its own 128-row MMA on W boxes multicast to
+ *                              both (an even number of batch tiles, D below
+ *                              4096 with two of them, below 6144 with more)
+ *   FS_STAGE1_PAIR_MMA         2-CTA clusters sharing one 256-row MMA
+ *                              (tcgen05 cta_group::2) for larger D
+ * Every form computes the same samples.  Returns FS_ERR_INVALID_ARG for a
+ * NULL out_form or a bad shape, FS_ERR_UNSUPPORTED / FS_ERR_CUDA when the
+ * current device is not an sm_103 GPU or cannot be queried.
+ * ------------------------------------------------------------------------- */
+enum { FS_STAGE1_ONE_CTA = 0, FS_STAGE1_MULTICAST_PAIR = 1, FS_STAGE1_PAIR_MMA = 2 };
+fs_status fs_stage1_form(int64_t B, int64_t V, int64_t D, int *out_form);
+
+/* ---------------------------------------------------------------------------
  * fs_sample_noalloc -- fs_sample that allocates no device memory.  The paper
  * has no counterpart: this is a library convenience.  It is for callers that
  * cannot allocate: applications that reserve all device memory up front and

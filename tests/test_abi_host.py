@@ -40,7 +40,7 @@ def test_header_declares_the_entry_points():
     for must in ("fs_sample", "fs_sample_ex", "fs_stage1", "fs_stage2", "fs_workspace_size",
                  "fs_logits_gemm", "fs_sample_from_logits", "fs_sample_unfused",
                  "fs_debug_noise", "fs_get_device_status", "fs_last_error_string",
-                 "fs_version", "fs_plan_info", "fs_release_workspaces"):
+                 "fs_version", "fs_plan_info", "fs_stage1_form", "fs_release_workspaces"):
         assert must in names
 
 
@@ -172,6 +172,22 @@ def test_valid_call_without_a_device_reports_cuda_error():
     UNSUPPORTED) instead of crashing: there is no CPU fallback."""
     st = call_sample()
     assert st in (_lib.FS_ERR_CUDA, _lib.FS_ERR_UNSUPPORTED)
+
+
+def test_stage1_form_validates_before_touching_a_device():
+    L = _lib.lib()
+    out = ctypes.c_int(-1)
+    assert L.fs_stage1_form(256, 4096, 64, None) == _lib.FS_ERR_INVALID_ARG
+    assert L.fs_stage1_form(0, 4096, 64, ctypes.byref(out)) == _lib.FS_ERR_INVALID_ARG
+    assert L.fs_stage1_form(256, 4096, 60, ctypes.byref(out)) == _lib.FS_ERR_UNSUPPORTED  # D % 8
+    assert out.value == -1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
+def test_stage1_form_without_a_device_reports_an_error():
+    out = ctypes.c_int(-1)
+    st = _lib.lib().fs_stage1_form(256, 4096, 64, ctypes.byref(out))
+    assert st in (_lib.FS_ERR_CUDA, _lib.FS_ERR_UNSUPPORTED) and out.value == -1
 
 
 def test_transformed_entry_validates():

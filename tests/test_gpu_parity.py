@@ -172,6 +172,17 @@ def test_ragged_shapes(fs, dev, B, V, D):
     run_and_check(fs, H, W, 0.9, 1000 + B, 3, "B=%d V=%d D=%d" % (B, V, D))
 
 
+@pytest.mark.parametrize("B,D,form", [
+    (64, 4096, 0), (100, 3584, 0), (384, 8192, 0),   # one or three batch tiles
+    (256, 3584, 1), (512, 2304, 1), (512, 4096, 1),  # pairs below the D switch
+    (256, 4096, 2), (256, 8192, 2), (512, 6144, 2), (1024, 8192, 2)])
+def test_stage1_form_rule(fs, dev, B, D, form):
+    """The launch form the library reports (and launches) for each shape:
+    pairs only for an even number of batch tiles, the pair MMA from D = 4096
+    with two batch tiles and from D = 6144 with more."""
+    assert fs.fs_stage1_form(B, 128256, D) == form
+
+
 def _random_shapes(n=48, seed=20261203):
     """Seeded (B, V, D) triples spread over the three launch forms: one batch
     tile, an odd number of batch tiles (unpaired), two and four batch tiles
