@@ -765,6 +765,61 @@ def test_transforms_match_oracle(fs, dev, B, V, D, softcap, use_bias, use_mask):
     print("[transforms B=%d V=%d] max |d logprob| = %.2e" % (B, V, err.max()))
 
 
+def _random_paired_shapes(n=12, seed=77031):
+    """Seeded paired shapes (two or four batch tiles, partial last tiles)
+    with D from 3584 to 8192 (both pair forms, the pair MMA with its column
+    hand-off) and a small V so that the oracle's full rows stay cheap."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for k in range(n):
+        B = int(rng.integers(129, 257)) if k % 2 == 0 else int(rng.integers(385, 513))
+        D = 8 * int(rng.integers(448, 1025))
+        V = int(rng.integers(40, 700))
+        out.append((B, V, D))
+    return out
+
+
+@pytest.mark.parametrize("k,B,V,D", [(k,) + s for k, s in enumerate(_random_paired_shapes())])
+def test_seeded_random_paired_logprob_and_transforms(fs, dev, k, B, V, D):
+    """Random paired shapes through the log-probability and transform modes
+    (with and without the log-mass): samples and log-probabilities against
+    the oracle on every row."""
+    rng = np.random.default_rng(900 + k)
+    g = torch.Generator(device="cpu").manual_seed(900 + k)
+    H = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn((V, D), generator=g) * (3.0 / D ** 0.5)).to(torch.bfloat16).to(dev)
+    T = torch.as_tensor(rng.uniform(0.5, 1.5, B).astype(np.float32))
+    l32 = oracle.logits(bits(H), bits(W))
+    # log-probability mode
+    idx, score, lp = fs.fs_sample_logprob(H, W, temperature=T.to(dev), seed=31 + k, offset=k)
+    torch.cuda.synchronize()
+    o_idx, o_best, o_second, _ = oracle.sample_from_logits(l32, T.numpy(), 31 + k, k)
+    g_idx = idx.cpu().numpy()
+    compare_indices(g_idx, o_idx, o_best, o_second, "logprob k=%d B=%d V=%d D=%d" % (k, B, V, D))
+    err = np.abs(lp.cpu().numpy() - oracle.logprob(l32, T.numpy(), g_idx))
+    assert np.all(err <= 2 * LOGIT_TOL / 0.5 + 1e-4), err.max()
+    # transform modes
+    bias = (rng.standard_normal(V) * 2).astype(np.float32)
+    mask = _mask(rng, B, V)
+    softcap = 20.0 if k % 3 else 0.0
+    tb = torch.as_tensor(bias).to(dev)
+    tm = torch.as_tensor(mask.view(np.int32)).to(dev)
+    i1, s1, lp1 = fs.fs_sample_transformed(H, W, bias=tb, softcap=softcap, allow_mask=tm,
+                                           temperature=T.to(dev), seed=57 + k, offset=2 * k,
+                                           want_logprob=True)
+    i2, s2, _ = fs.fs_sample_transformed(H, W, bias=tb, softcap=softcap, allow_mask=tm,
+                                         temperature=T.to(dev), seed=57 + k, offset=2 * k)
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2) and torch.equal(s1, s2)
+    lx = oracle.transform_logits(l32, bias, softcap, mask)
+    o_idx, o_best, o_second, _ = oracle.sample_from_logits(lx, T.numpy(), 57 + k, 2 * k)
+    g_idx = i1.cpu().numpy()
+    compare_indices(g_idx, o_idx, o_best, o_second, "transforms k=%d B=%d V=%d D=%d" % (k, B, V, D))
+    live = g_idx >= 0
+    err = np.abs(lp1.cpu().numpy()[live] - oracle.logprob(lx, T.numpy(), g_idx)[live])
+    assert np.all(err <= 2 * LOGIT_TOL / 0.5 + 1e-4), err.max()
+
+
 def test_zero_transforms_equal_plain_sampling_and_full_mask(fs, dev):
     B, V, D = 70, 30011, 192
     g = torch.Generator(device="cpu").manual_seed(77)
